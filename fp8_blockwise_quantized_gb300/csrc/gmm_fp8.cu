@@ -1,0 +1,342 @@
+// a4-a6: FP8 blockwise grouped GEMM forward on the 5th-generation tensor core.
+//
+// What it computes ("GEMM Kernel 性能优化十问", Q1/Q3; "实现差距：GMM Kernel
+// （V1 vs V2）", §3.3 and §3.5): for the row tile (g, row0..row1) and a column
+// block, for every 128-wide K block kb (one LHS / RHS quantization block) the
+// exact FP8 partial P_kb = Xq[rows, kb] . Wq[g][kb, cols] is formed in fp32 and
+// promoted into the accumulator with the LHS row scale times the RHS block
+// scale: acc += P_kb * xs[kb, m] * ws[g, kb, n/128].  The output is bf16(acc),
+// or bf16(silu(acc_gate) * acc_up) with the fused gate/up weight.
+//
+// How (sm_103a).  The quantization block is decoupled from the pipeline: the
+// MMA never stops at a block boundary, only its accumulator buffer changes.
+//   warp 0      TMA producer: per K block one 128x128 B Xq tile and one
+//               BNx128 B Wq tile (K-major, 128-byte swizzle) into a 4-stage
+//               shared-memory ring, completion counted on an mbarrier.
+//   warp 1      allocates TMEM and issues tcgen05.mma (kind::f8f6f4, M=128,
+//               N=BN, K=32, four per K block) into one of two TMEM partial
+//               buffers; tcgen05.commit frees the ring slot and publishes the
+//               partial.
+//   warps 2-3   idle (they complete warpgroup 0, which hands most of its
+//               registers to the promotion warpgroups).
+//   warps 4-11  promotion: tcgen05.ld the partial (one TMEM lane = one row),
+//               FMA it into fp32 registers with the scale product, release the
+//               buffer; after the last K block convert and store the rows
+//               row0..row1 of the tile (masked: the tile may run into the next
+//               group), and zero the output rows that no group covers.
+// Work units (tile, column block) are dealt round-robin to a persistent grid
+// of one CTA per SM, tile-major so that the units sharing an Xq tile and the
+// tiles sharing an expert's Wq columns run at the same time (L2 reuse).
+// Every wait is bounded; a timeout sets the workspace error word and all
+// roles unwind, wait for their copies and MMAs in flight and free TMEM.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace gmm {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+constexpr int kPromoWarps = 8;
+constexpr int kPromoWarp0 = 4;   // first promotion warp
+// Register split: the launch gives 168 registers per thread (three warps per
+// SM sub-partition); warpgroup 0 (TMA, MMA, two idle warps) gives most of its
+// share to the two promotion warpgroups, which hold the fp32 accumulators:
+// 128 x control + 256 x promo <= 384 x 168 = 64512.
+template <int BN>
+struct RegSplit {
+  static constexpr uint32_t kControl = BN == 256 ? 40 : 72;
+  static constexpr uint32_t kPromo = BN == 256 ? 232 : 216;
+  static_assert(128 * kControl + 256 * kPromo <= 384 * 168, "register split exceeds the launch budget");
+};
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+template <int BN, bool FUSE>
+struct Fp8Tile {
+  static constexpr int kABytes = kBM * 128;
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSeg = BN / 4;                  // columns per accumulator segment
+  static constexpr int kOutCols = FUSE ? BN / 2 : BN;  // output columns per work unit
+  static constexpr int kTmemCols = 2 * BN;             // two partial buffers
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+};
+
+template <int BN, bool FUSE>
+__global__ void __launch_bounds__(kThreads, 1)
+    gmm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const FwdArgs args) {
+  using C = Fp8Tile<BN, FUSE>;
+  constexpr int SEG = C::kSeg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kPromoWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const int num_tiles = args.meta[kWsNumTiles];
+  const int units_per_tile = args.N / C::kOutCols;
+  const long long num_units = static_cast<long long>(num_tiles) * units_per_tile;
+  const int KB = args.K / 128;
+  const int Nw = FUSE ? 2 * args.N : args.N;
+  const uint64_t lim = args.wait_limit_ns;
+
+  if (warp < kPromoWarp0) regs_dec<RegSplit<BN>::kControl>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t c = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const Tile tl = args.tiles[u / units_per_tile];
+        const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+        const int brow = tl.g * Nw + n0;
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_word, lim)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = ring + s * C::kStageBytes;
+          uint8_t* b_dst = a_dst + C::kABytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          tma_load_2d(a_dst, &map_a, &full[s], kb * 128, tl.row0);
+          if (FUSE) {
+            tma_load_2d(b_dst, &map_b, &full[s], kb * 128, brow);
+            tma_load_2d(b_dst + C::kBBytes / 2, &map_b, &full[s], kb * 128, brow + args.N);
+          } else {
+            tma_load_2d(b_dst, &map_b, &full[s], kb * 128, brow);
+          }
+          ++c;
+        }
+      }
+      // wait for the last copy issued into every slot (they land in microseconds)
+      volatile int no_abort = 0;
+      for (uint32_t s = 0; s < kStages; ++s) {
+        if (c > s) {
+          const uint32_t last = s + kStages * ((c - 1 - s) / kStages);
+          mbar_wait(&full[s], (last / kStages) & 1u, &no_abort, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(0u /*e4m3*/, false, false, kBM, BN);
+      uint32_t c = 0, t = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_word, lim)) {
+            ok = false;
+            break;
+          }
+          const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+          if (!mbar_wait(&tempty[b], tph ^ 1u, abort_word, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(ring + s * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+          const uint32_t d = tbase + b * BN;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            mma_f8(d, smem_desc_sw128(a_addr + 32 * j, 16, 1024), smem_desc_sw128(b_addr + 32 * j, 16, 1024),
+                   idesc, j > 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+          mma_commit(&tfull[b]);
+          ++c;
+          ++t;
+        }
+      }
+      if (c > 0) {
+        volatile int no_abort = 0;
+        mma_commit(drain);
+        mbar_wait(drain, 0, &no_abort, kDrainLimitNs);
+      }
+    }
+  } else if (warp >= kPromoWarp0) {
+    // ------------------------------------------------------------ promotion + epilogue
+    regs_inc<RegSplit<BN>::kPromo>();
+    const int pw = warp - kPromoWarp0;
+    const int h = pw >> 2;        // column half of the tile
+    const int quad = warp & 3;    // TMEM lane quadrant this warp may access
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+
+    // rows [S, M) belong to no group: zero them (spread over the whole grid)
+    {
+      const int S = args.meta[kWsS];
+      if (S < args.M) {
+        const long long total = static_cast<long long>(args.M - S) * args.N / 8;
+        uint4* p = reinterpret_cast<uint4*>(args.out + static_cast<long long>(S) * args.N);
+        const long long stride = static_cast<long long>(gridDim.x) * (kPromoWarps * 32);
+        for (long long i = static_cast<long long>(blockIdx.x) * (kPromoWarps * 32) + (threadIdx.x - kPromoWarp0 * 32);
+             i < total;
+             i += stride)
+          p[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+
+    const int NBw = Nw / 128;
+    uint32_t t = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Tile tl = args.tiles[u / units_per_tile];
+      const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+      const int row = tl.row0 + quad * 32 + lane;
+      const bool valid = row < tl.row1;
+      int tcol0, tcol1, wblk0, wblk1;
+      if (FUSE) {
+        tcol0 = h * SEG;
+        tcol1 = BN / 2 + h * SEG;
+        wblk0 = n0 / 128;
+        wblk1 = (args.N + n0) / 128;
+      } else {
+        tcol0 = h * (BN / 2);
+        tcol1 = h * (BN / 2) + SEG;
+        wblk0 = wblk1 = (n0 + h * (BN / 2)) / 128;
+      }
+      const float* xs_p = args.xs + (valid ? row : 0);
+      const float* ws_p = args.ws + static_cast<long long>(tl.g) * KB * NBw;
+
+      float acc[2 * SEG];
+#pragma unroll
+      for (int i = 0; i < 2 * SEG; ++i) acc[i] = 0.0f;
+
+      float sx_n = valid ? __ldg(xs_p) : 0.0f;
+      float sw0_n = __ldg(ws_p + wblk0), sw1_n = __ldg(ws_p + wblk1);
+      for (int kb = 0; kb < KB; ++kb) {
+        const float sx = sx_n, sw0 = sw0_n, sw1 = sw1_n;
+        if (kb + 1 < KB) {
+          sx_n = valid ? __ldg(xs_p + static_cast<long long>(kb + 1) * args.M) : 0.0f;
+          sw0_n = __ldg(ws_p + (kb + 1) * NBw + wblk0);
+          sw1_n = __ldg(ws_p + (kb + 1) * NBw + wblk1);
+        }
+        const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+        const bool got = mbar_wait(&tfull[b], tph, abort_word, lim);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f0 = sx * sw0, f1 = sx * sw1;
+        const uint32_t tb = t_lane + b * BN;
+#pragma unroll
+        for (int cc = 0; cc < SEG / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32(tb + tcol0 + 32 * cc, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 * cc + i] = fmaf(__uint_as_float(r[i]), f0, acc[32 * cc + i]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < SEG / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld_32x32(tb + tcol1 + 32 * cc, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            acc[SEG + 32 * cc + i] = fmaf(__uint_as_float(r[i]), f1, acc[SEG + 32 * cc + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        ++t;
+      }
+      if (!ok) break;
+      if (valid) {
+        uint16_t* orow = args.out + static_cast<long long>(row) * args.N;
+        if (FUSE) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * SEG);
+#pragma unroll
+          for (int j = 0; j < SEG; j += 8) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = silu_f32(acc[j + i]) * acc[SEG + j + i];
+            dst[j / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                    pack_bf16x2(v[6], v[7]));
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * (BN / 2));
+#pragma unroll
+          for (int j = 0; j < 2 * SEG; j += 8) {
+            dst[j / 8] = make_uint4(pack_bf16x2(acc[j], acc[j + 1]), pack_bf16x2(acc[j + 2], acc[j + 3]),
+                                    pack_bf16x2(acc[j + 4], acc[j + 5]), pack_bf16x2(acc[j + 6], acc[j + 7]));
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
+}
+
+template <int BN, bool FUSE>
+cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
+                   cudaStream_t stream) {
+  constexpr int smem = Fp8Tile<BN, FUSE>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(gmm_fp8_kernel<BN, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  gmm_fp8_kernel<BN, FUSE><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+Fp8Geometry fp8_geometry(int N, int fuse) {
+  if (fuse) return {256, 128, 128};
+  if (N % 256 == 0) return {256, 256, 256};
+  return {128, 128, 128};
+}
+
+cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
+                           cudaStream_t stream) {
+  if (args.fuse) return launch<256, true>(map_a, map_b, args, grid, stream);
+  if (args.N % 256 == 0) return launch<256, false>(map_a, map_b, args, grid, stream);
+  return launch<128, false>(map_a, map_b, args, grid, stream);
+}
+
+}  // namespace gmm

@@ -1,0 +1,58 @@
+// Kernel entry points and their host-side launchers (internal to the library).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gmm {
+
+// ---- a1 metadata ------------------------------------------------------------
+__global__ void group_metadata_kernel(const int32_t* sizes, int G, int M, int32_t* ws, Tile* tiles);
+
+// ---- a2 / a3 quantization -----------------------------------------------------
+constexpr int kLhsBlocksPerWarp = 8;
+__global__ void quantize_lhs_kernel(const uint4* x, int M, int KB, long long nblocks, uint2* xq, float* xs);
+__global__ void quantize_rhs_kernel(const uint16_t* w, int K, int N, uint8_t* wq, float* ws);
+
+// ---- grouped GEMMs ------------------------------------------------------------
+// Arguments shared by the grouped forward kernels.
+struct FwdArgs {
+  const float* xs;        // fp32 [K/128][M] (FP8 only)
+  const float* ws;        // fp32 [G][K/128][Nw/128] (FP8 only)
+  const int32_t* meta;    // workspace words
+  const Tile* tiles;      // workspace tile list
+  uint16_t* out;          // bf16 [M][N]
+  int M, K, N;            // N = output columns
+  int fuse;               // 1: silu(gate) * up, W has 2N columns
+  uint64_t wait_limit_ns;
+};
+
+struct TgmmArgs {
+  const int32_t* meta;    // workspace words (offsets)
+  uint16_t* dw;           // bf16 [G][K][N]
+  int G, M, K, N;
+  uint64_t wait_limit_ns;
+};
+
+// Host launchers: `grid` CTAs (persistent), on `stream`.  Return the launch error.
+cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args,
+                             int grid, cudaStream_t stream);
+
+// Tile geometry the host needs to build tensor maps and size grids.
+struct Fp8Geometry {
+  int bn_mma;      // MMA N (columns of W per stage)
+  int out_cols;    // output columns per work unit
+  int b_box_rows;  // rows of the W tensor-map box
+};
+Fp8Geometry fp8_geometry(int N, int fuse);
+Fp8Geometry bf16_geometry(int N, int fuse);
+int tgmm_bn(int N);
+
+}  // namespace gmm

@@ -1,0 +1,253 @@
+// a8: tgmm, the expert weight gradient in bf16.
+//
+// dW[g][k, n] = sum over the rows m of group g of x[m, k] * dy[m, n]
+// ("GEMM Kernel 性能优化十问", Q4: dW[K,N] += X^T[K,M] dY[M,N], M is the
+// reduction dimension; Q5: the backward pass is not quantized).  fp32
+// accumulation, bf16 output; an empty group gets dW[g] = 0.
+//
+// Work unit = one output tile (g, 128 rows of K, BN columns of N).  Its
+// reduction walks the group's rows in chunks of 64:
+//   warp 0     TMA: x[rows, 128 k] as two 64x64 boxes and dy[rows, BN n] as
+//              BN/64 boxes; both land MN-major (K of the MMA = the row index).
+//   warp 1     on the group's last, partial chunk, zeroes the dy rows that
+//              belong to the next group (whole 128-byte rows, so the swizzle
+//              does not matter) and fences them into the async proxy; then
+//              tcgen05.mma kind::f16, M=128 (k), N=BN (n), K=16 (rows).
+//   warps 2-9  epilogue: tcgen05.ld -> bf16 -> dW rows; zero tile for an
+//              empty group.
+// TMEM holds two accumulators, so one tile's epilogue overlaps the next
+// tile's MMAs.  Units are ordered group-major so the tiles of one group (which
+// share its x and dy rows) run together.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace gmm {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kChunk = 64;  // rows per stage
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+template <int BN>
+struct TgmmTile {
+  static constexpr int kBoxBytes = kChunk * 64 * 2;  // 64 rows x 64 bf16 = 8 KB
+  static constexpr int kABytes = 2 * kBoxBytes;      // 128 k columns
+  static constexpr int kBBytes = (BN / 64) * kBoxBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tgmm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dy,
+                const TgmmArgs args) {
+  using C = TgmmTile<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_dy);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const bool valid_meta = args.meta[kWsValid] != 0;
+  const int KT = args.K / 128, NT = args.N / BN;
+  const long long num_units = valid_meta ? static_cast<long long>(args.G) * KT * NT : 0;
+  const int* offsets = args.meta + kWsOffsets;
+  const uint64_t lim = args.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t c = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int g = static_cast<int>(u / (KT * NT));
+        const int rem = static_cast<int>(u % (KT * NT));
+        const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
+        const int r0 = offsets[g], r1 = offsets[g + 1];
+        for (int r = r0; r < r1; r += kChunk) {
+          const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_word, lim)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = ring + s * C::kStageBytes;
+          uint8_t* b_dst = a_dst + C::kABytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          tma_load_2d(a_dst, &map_x, &full[s], k0, r);
+          tma_load_2d(a_dst + C::kBoxBytes, &map_x, &full[s], k0 + 64, r);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) tma_load_2d(b_dst + i * C::kBoxBytes, &map_dy, &full[s], n0 + 64 * i, r);
+          ++c;
+        }
+      }
+      volatile int no_abort = 0;
+      for (uint32_t s = 0; s < kStages; ++s) {
+        if (c > s) {
+          const uint32_t last = s + kStages * ((c - 1 - s) / kStages);
+          mbar_wait(&full[s], (last / kStages) & 1u, &no_abort, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // the whole warp walks the loop: lanes help zero foreign rows
+    constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, kBM, BN);
+    uint32_t c = 0, t = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const int g = static_cast<int>(u / (KT * NT));
+      const int r0 = offsets[g], r1 = offsets[g + 1];
+      if (r1 <= r0) continue;  // empty group: the epilogue writes zeros
+      const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[b], tph ^ 1u, abort_word, lim))) break;
+      tc_fence_after();
+      const uint32_t d = tbase + b * BN;
+      for (int r = r0; r < r1; r += kChunk) {
+        const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_word, lim))) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_ptr = ring + s * C::kStageBytes;
+        uint8_t* b_ptr = a_ptr + C::kABytes;
+        const int live = r1 - r;  // rows of this chunk that belong to group g
+        if (live < kChunk) {
+          // zero dy rows [live, 64) of every box: 128 bytes per row
+          const int nbytes16 = (kChunk - live) * 8;  // 16-byte words per box
+          for (int i = 0; i < BN / 64; ++i) {
+            uint4* p = reinterpret_cast<uint4*>(b_ptr + i * C::kBoxBytes + live * 128);
+            for (int w = lane; w < nbytes16; w += 32) p[w] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(a_ptr);
+          const uint32_t b_addr = smem_u32(b_ptr);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            mma_bf16(d, smem_desc_sw128(a_addr + 2048 * j, C::kBoxBytes, 1024),
+                     smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024), idesc, (r > r0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        __syncwarp();
+        ++c;
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&tfull[b]);
+      __syncwarp();
+      ++t;
+    }
+    if (lane == 0 && c > 0) {
+      volatile int no_abort = 0;
+      mma_commit(drain);
+      mbar_wait(drain, 0, &no_abort, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    const int pw = warp - 2;
+    const int h = pw >> 2;
+    const int quad = warp & 3;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    uint32_t t = 0;
+    for (long long u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const int g = static_cast<int>(u / (KT * NT));
+      const int rem = static_cast<int>(u % (KT * NT));
+      const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
+      const int r0 = offsets[g], r1 = offsets[g + 1];
+      const long long krow = static_cast<long long>(g) * args.K + k0 + quad * 32 + lane;
+      uint4* dst = reinterpret_cast<uint4*>(args.dw + krow * args.N + n0 + h * (BN / 2));
+      if (r1 <= r0) {
+#pragma unroll
+        for (int j = 0; j < BN / 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, abort_word, lim))) break;
+      tc_fence_after();
+      const uint32_t tb = t_lane + b * BN + h * (BN / 2);
+#pragma unroll
+      for (int cc = 0; cc < BN / 64; ++cc) {
+        uint32_t r[32];
+        tmem_ld_32x32(tb + 32 * cc, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          dst[cc * 4 + j / 8] = make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                           pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                           pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                                           pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      ++t;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
+}
+
+template <int BN>
+cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args, int grid,
+                   cudaStream_t stream) {
+  constexpr int smem = TgmmTile<BN>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(tgmm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tgmm_kernel<BN><<<grid, kThreads, smem, stream>>>(map_x, map_dy, args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int tgmm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
+
+cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args, int grid,
+                             cudaStream_t stream) {
+  if (args.N % 256 == 0) return launch<256>(map_x, map_dy, args, grid, stream);
+  return launch<128>(map_x, map_dy, args, grid, stream);
+}
+
+}  // namespace gmm

@@ -1,0 +1,166 @@
+/*
+ * gmm.h — C ABI of the GB300 (sm_103a) MoE grouped matmul library.
+ *
+ * The operation (a grouped matrix multiply, "GMM"): the rows of an activation
+ * matrix X[M,K] are sorted by expert into G contiguous groups of sizes
+ * group_sizes[0..G); group g owns rows [off_g, off_g + n_g), off being the
+ * exclusive prefix sum of the sizes, and is multiplied by its own expert
+ * weight W[g][K,N] ("MoE 优化的探索", §3.7.2: a grouped GEMM is a set of
+ * independent per-expert GEMMs scheduled in one kernel; "GEMM Kernel
+ * 性能优化十问", Q6 for the shapes).  Output rows from S = sum(group_sizes) up
+ * to M belong to no group and are written as zeros ("实现差距：GMM Kernel（V1
+ * vs V2）", §3.6).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless stated otherwise.  The caller owns
+ *     every buffer (including the workspace); the library never allocates
+ *     device memory.  Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they validate their arguments on the
+ *     host, enqueue kernels on `stream` and return.
+ *   - Host-checked errors (null pointer, shape, alignment, workspace size)
+ *     return immediately and launch nothing.
+ *   - Data-dependent errors (a negative group size, sum(group_sizes) > M) and
+ *     a kernel's bounded wait running out set a sticky error word inside the
+ *     workspace; the kernels then stop early and the outputs are undefined.
+ *     gmm_get_device_status() reads and clears that word.  No kernel traps.
+ *   - Row-major layouts; bf16 = IEEE bfloat16; e4m3 = OCP FP8 E4M3 (max 448).
+ *   - K and N are multiples of 128 (the quantization block); 1 <= G <= 4096;
+ *     0 <= M < 2^31.  M = 0, or every group empty, is valid.
+ */
+#ifndef GMM_GB300_H
+#define GMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GMM_OK = 0,
+  GMM_ERR_NULL = 1,         /* a required pointer is NULL */
+  GMM_ERR_SHAPE = 2,        /* a size is out of range or not a multiple of 128 */
+  GMM_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+  GMM_ERR_UNSUPPORTED = 4,  /* no GPU of compute capability 10.3 is current */
+  GMM_ERR_CUDA = 5,         /* a CUDA runtime / driver call failed */
+  GMM_ERR_GROUP_SIZES = 6,  /* device-detected: negative size or sum > M */
+  GMM_ERR_TIMEOUT = 7,      /* device-detected: a bounded wait ran out */
+  GMM_ERR_WORKSPACE = 8     /* workspace NULL or smaller than gmm_workspace_bytes */
+} gmm_status;
+
+/* Human-readable name of a status code (static storage). */
+const char* gmm_status_string(gmm_status status);
+
+/* Message of the last CUDA error seen by this thread's calls (static storage). */
+const char* gmm_last_cuda_error(void);
+
+/*
+ * Bytes of device workspace the grouped calls need for G groups and M rows:
+ * a status word, the group offsets and the row-tile list.  The workspace must
+ * be zero-filled once before its first use (its first word is the sticky
+ * error word); afterwards it may be reused by any number of calls issued on
+ * one stream.  Two calls that run concurrently need two workspaces.
+ */
+size_t gmm_workspace_bytes(int G, int64_t M);
+
+/*
+ * a1 — group metadata.  ("MoE 优化的探索", §3.7.2: tiles carry their expert id
+ * and are located through offsets; "实现差距：GMM Kernel（V1 vs V2）", §1/§2.2:
+ * the metadata is filled on the device.)
+ * Reads group_sizes int32[G] (device) and writes into `workspace`:
+ *   int32 word[0]  sticky error bits (1: a negative size, 2: sum > M,
+ *                  4: a bounded wait ran out), OR-ed, never cleared here
+ *   int32 word[1]  1 if this call's sizes were valid, else 0
+ *   int32 word[2]  S = sum(group_sizes)        (M when invalid)
+ *   int32 word[3]  T = number of row tiles      (0 when invalid)
+ *   int32 word[8 + g], g = 0..G  exclusive prefix sums off_g (off_G = S)
+ *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
+ *                  every group cut into consecutive tiles of at most 128 rows,
+ *                  groups in order, empty groups contributing none.
+ * The grouped calls below run this step themselves; it is exported so that
+ * it can be checked and timed on its own.
+ */
+gmm_status gmm_group_metadata(const int32_t* group_sizes, int G, int64_t M, void* workspace,
+                              size_t workspace_bytes, void* stream);
+size_t gmm_tiles_offset(int G);
+
+/*
+ * a2 — dynamic LHS quantization in 1x128 blocks ("GEMM Kernel 性能优化十问",
+ * Q2: one scale per row per 128 elements; "实现差距：GMM Kernel（V1 vs V2）",
+ * §3.3: absmax -> scale = absmax / 448 -> inv = (scale == 0 ? 0 : 1/scale)
+ * -> q = e4m3(x * inv)).  Scale and product are IEEE fp32, rounding to
+ * nearest; the e4m3 cast rounds to nearest even and saturates at 448.
+ *   x   bf16 [M, K]
+ *   xq  e4m3 [M, K]            (one byte per element)
+ *   xs  fp32 [K/128, M]        (scale of row m, block kb at xs[kb*M + m])
+ */
+gmm_status gmm_quantize_lhs(const void* x, int64_t M, int64_t K, void* xq, float* xs, void* stream);
+
+/*
+ * a3 — offline RHS quantization in 128x128 blocks (Q2: weights are static,
+ * one scale per 128x128 block, computed ahead of time), same per-block rule.
+ *   w   bf16 [G, K, N]
+ *   wq  e4m3 [G, N, K]   NOTE: transposed ("K-major"): wq[(g*N + n)*K + k]
+ *                        holds the code of w[g][k][n]
+ *   ws  fp32 [G, K/128, N/128]
+ * For the fused gate/up weight pass N = 2 * N_out (gate columns first).
+ */
+gmm_status gmm_quantize_rhs(const void* w, int G, int64_t K, int64_t N, void* wq, float* ws, void* stream);
+
+/*
+ * a4-a6 — FP8 blockwise GMM forward ("GEMM Kernel 性能优化十问", Q1/Q3: the
+ * K loop runs over many 128-wide quantization blocks; each block's exact
+ * partial product is promoted into an fp32 accumulator with the LHS row scale
+ * times the RHS block scale; "实现差距：GMM Kernel（V1 vs V2）", §3.3):
+ *   out[m,n] = bf16( sum_kb P_kb[m,n] * xs[kb,m] * ws[g,kb,n/128] ),
+ *   P_kb[m,n] = sum_{k in kb} xq[m,k] * wq[g,k,n]   (fp32 on the tensor core)
+ * fuse_silu_mul = 1 (§3.5 of the V1/V2 page): wq holds 2N columns (gate
+ * [0,N), up [N,2N)) and out[m,n] = bf16(silu(y_gate) * y_up), silu(v) =
+ * v / (1 + exp(-v)), applied to the fp32 accumulators.
+ *   xq, xs    as written by gmm_quantize_lhs (M rows, K columns)
+ *   wq, ws    as written by gmm_quantize_rhs (G, K, N or 2N)
+ *   out       bf16 [M, N]; rows >= S are written as zeros
+ */
+gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const float* ws,
+                       const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
+                       int fuse_silu_mul, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * a7 — bf16 GMM forward, unquantized (the BF16 baseline of "GEMM Kernel
+ * 性能优化十问", Q7/Q10 step 4): out[m,n] = bf16(sum_k x[m,k] * w[g,k,n]),
+ * fp32 accumulation; fuse_silu_mul as for gmm_fp8_fwd.
+ *   x    bf16 [M, K]
+ *   w    bf16 [G, K, N or 2N]   (natural layout, N contiguous)
+ *   out  bf16 [M, N]; rows >= S are written as zeros
+ */
+gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes, int G, int64_t M,
+                        int64_t K, int64_t N, int fuse_silu_mul, void* out, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
+ * a8 — tgmm, the expert weight gradient ("GEMM Kernel 性能优化十问", Q4:
+ * dW[K,N] += X^T[K,M] dY[M,N], M is the reduction; Q5: the backward pass
+ * stays bf16, unquantized):
+ *   dw[g][k,n] = bf16( sum_{m in group g} x[m,k] * dy[m,n] ), fp32 accumulation;
+ *   dw[g] = 0 for an empty group.
+ *   x   bf16 [M, K];  dy  bf16 [M, N];  dw  bf16 [G, K, N]
+ */
+gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M,
+                     int64_t K, int64_t N, void* dw, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
+ * Synchronizes `stream`, reads the workspace's sticky error word, clears it
+ * and maps it to a status: GMM_ERR_TIMEOUT if a wait ran out, else
+ * GMM_ERR_GROUP_SIZES if some call saw invalid group sizes, else GMM_OK.
+ */
+gmm_status gmm_get_device_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMM_GB300_H */
