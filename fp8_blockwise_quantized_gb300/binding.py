@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_
 
 EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "gmm_tiles_offset",
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
-            "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status"]
+            "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc"]
 
 
 class GmmError(RuntimeError):
@@ -74,6 +74,8 @@ def load():
     lib.tgmm_bf16.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
     lib.gmm_get_device_status.restype = I
     lib.gmm_get_device_status.argtypes = [P, P]
+    lib.gmm_fp8_fwd_noalloc.restype = I
+    lib.gmm_fp8_fwd_noalloc.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P]
     _lib = lib
     return lib
 
@@ -142,6 +144,14 @@ def tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, st
 
 def gmm_get_device_status(workspace, stream=None) -> int:
     return load().gmm_get_device_status(_p(workspace), _s(stream))
+
+
+def gmm_fp8_fwd_noalloc(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out,
+                        stream=None) -> int:
+    """gmm_fp8_fwd for callers that cannot allocate: no workspace argument;
+    the metadata lives in the library's static device array (see gmm.h)."""
+    return load().gmm_fp8_fwd_noalloc(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
+                                      int(fuse_silu_mul), _p(out), _s(stream))
 
 
 # ---------------------------------------------------------------------------

@@ -153,6 +153,39 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
                      void* stream);
 
 /*
+ * gmm_fp8_fwd without a workspace argument, for callers that cannot allocate
+ * device memory when they run the layer: code running under a framework whose
+ * allocator owns all device memory, a runtime that must not allocate after
+ * start-up (fixed budgets, real-time loops), or a plug-in that is only handed
+ * its input and output buffers.  (The pages have no counterpart: this is an
+ * interface choice of this library, not part of the method.)
+ *
+ * Same arguments, layouts and result as gmm_fp8_fwd, minus the workspace.
+ * The group metadata goes to a 64 KiB array in the library's own device
+ * memory (a file-scope __device__ variable, reserved on every GPU that loads
+ * the library and held until the process exits).  The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Limit: gmm_workspace_bytes(G, M) must be <= 65536 (for example G <= 1024
+ *     with M <= 262144); larger sizes return GMM_ERR_WORKSPACE and launch
+ *     nothing.
+ *   - The first call on each device does a one-time set-up with that device
+ *     current (it looks up the device address of the array with
+ *     cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents for
+ *     the next; each call rewrites all it reads.  Calls that overlap on the
+ *     GPU (different streams without ordering between them) race on it and
+ *     must not be issued.
+ *   - Device-detected errors (invalid group_sizes, a wait that ran out) are
+ *     not reported by this entry point: the array's error word is cleared at
+ *     the start of every call and cannot be read through this ABI; on such an
+ *     error the output is undefined.  Validate group_sizes beforehand, or use
+ *     gmm_fp8_fwd with a workspace and gmm_get_device_status.
+ */
+gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const void* wq, const float* ws,
+                               const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
+                               int fuse_silu_mul, void* out, void* stream);
+
+/*
  * Synchronizes `stream`, reads the workspace's sticky error word, clears it
  * and maps it to a status: GMM_ERR_TIMEOUT if a wait ran out, else
  * GMM_ERR_GROUP_SIZES if some call saw invalid group sizes, else GMM_OK.
