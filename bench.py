@@ -507,6 +507,61 @@ def run_reference(args):
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------------------
+# single-kernel mode for profilers: production shapes, only what one kernel needs
+# ---------------------------------------------------------------------------
+
+def run_profile_case(args):
+    import torch
+    import fp8_blockwise_quantized_gb300 as gmm
+    from fp8_blockwise_quantized_gb300.build import build
+    from fp8_blockwise_quantized_gb300.workloads import routing_sizes
+    build()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2024)
+    sizes = torch.from_numpy(routing_sizes("prod_fp8")).to(dev)
+    work = gmm.Workspace(G, M, dev)
+    chk = gmm.binding._check
+    case = args.profile_case
+
+    def bf16(shape, std=1.0):
+        return (torch.randn(shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    if case in ("fp8_wi", "fp8_wo"):
+        k, n, fuse = (K, N, 1) if case == "fp8_wi" else (N, K, 0)
+        x = bf16((M, k))
+        xq, xs = gmm.quantize_lhs(x)
+        w = bf16((G, k, 2 * n if fuse else n), 1.0 / math.sqrt(k))
+        wq, ws = gmm.quantize_rhs(w)
+        del x, w
+        out = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        run = lambda: chk(gmm.gmm_fp8_fwd(xq, xs, wq, ws, sizes, G, M, k, n, fuse, out, work.buf,
+                                          work.nbytes, None), case)
+    elif case in ("tgmm_wi", "tgmm_wo"):
+        k, n = (K, 2 * N) if case == "tgmm_wi" else (N, K)
+        x = bf16((M, k))
+        dy = bf16((M, n))
+        dw = torch.empty((G, k, n), dtype=torch.bfloat16, device=dev)
+        run = lambda: chk(gmm.tgmm_bf16(x, dy, sizes, G, M, k, n, dw, work.buf, work.nbytes, None), case)
+    elif case == "quantize_x":
+        x = bf16((M, K))
+        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        xs = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        run = lambda: chk(gmm.gmm_quantize_lhs(x, M, K, xq, xs, None), case)
+    else:
+        raise SystemExit(f"unknown profile case {case}")
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    st = work.status()
+    print(json.dumps({"profile_case": case, "launches": args.warmup + args.steps, "status": st}))
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -517,11 +572,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bf16-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    choices=["fp8_wi", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
+                    help="run one kernel at the production shape (for ncu) and exit")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured for this build")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.profile_case:
         ap.error("--warmup must be >= 3")
+    if args.profile_case:
+        run_profile_case(args)
+        return
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
