@@ -10,7 +10,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gmm.h"
+#include "gmm.h"
 #include "common.cuh"
 #include "kernels.cuh"
 

@@ -17,7 +17,11 @@
 //               N=BN, K=32, four per K block) into one of two TMEM partial
 //               buffers; tcgen05.commit frees the ring slot and publishes the
 //               partial.
-//   warps 2-3   idle (they complete warpgroup 0, which hands most of its
+//   warp 2      scale loader: per K block, cp.async copies of the tile's 128
+//               row scales xs[kb, rows] and its RHS block scales into a
+//               shared-memory ring that runs ahead of the MMAs (the scales are
+//               then never a global-memory load on the promotion's path).
+//   warp 3      idle (completes warpgroup 0, which hands most of its
 //               registers to the promotion warpgroups).
 //   warps 4-11  promotion: tcgen05.ld the partial (one TMEM lane = one row),
 //               FMA it into fp32 registers with the scale product, release the
@@ -52,6 +56,8 @@ struct RegSplit {
   static_assert(128 * kControl + 256 * kPromo <= 384 * 168, "register split exceeds the launch budget");
 };
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr int kScaleSlots = 8;        // K blocks of scales in flight
+constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
 
 template <int BN, bool FUSE>
 struct Fp8Tile {
@@ -61,8 +67,9 @@ struct Fp8Tile {
   static constexpr int kSeg = BN / 4;                  // columns per accumulator segment
   static constexpr int kOutCols = FUSE ? BN / 2 : BN;  // output columns per work unit
   static constexpr int kTmemCols = 2 * BN;             // two partial buffers
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kScaleBytes + kBarBytes;
 };
 
 template <int BN, bool FUSE>
@@ -74,11 +81,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  float* scales = reinterpret_cast<float*>(smem + kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes + C::kScaleBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + kScaleSlots;
+  uint64_t* drain = sempty + kScaleSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -91,6 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kPromoWarps);
+    }
+    for (int q = 0; q < kScaleSlots; ++q) {
+      mbar_init(&sfull[q], 32);  // one cp.async arrival per loader lane
+      mbar_init(&sempty[q], kPromoWarps);
     }
     mbar_init(drain, 1);
     *abort_word = 0;
@@ -191,6 +205,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(drain, 0, &no_abort, kDrainLimitNs);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale loader
+    const int NBw = Nw / 128;
+    uint32_t q = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Tile tl = args.tiles[u / units_per_tile];
+      const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+      // the (up to) two RHS column blocks this unit's accumulators use
+      const int wb0 = n0 / 128;
+      const int wb1 = FUSE ? (args.N + n0) / 128 : (BN == 256 ? n0 / 128 + 1 : n0 / 128);
+      const float* ws_g = args.ws + static_cast<long long>(tl.g) * KB * NBw;
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t sl = q % kScaleSlots, ph = (q / kScaleSlots) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&sempty[sl], ph ^ 1u, abort_word, lim))) {
+          ok = false;
+          break;
+        }
+        float* slot = scales + sl * kScaleSlotFloats;
+        const float* xs_kb = args.xs + static_cast<long long>(kb) * args.M;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = lane * 4 + j;
+          if (tl.row0 + r < args.M) cp_async_4(slot + r, xs_kb + tl.row0 + r);
+        }
+        if (lane == 0) {
+          cp_async_4(slot + 128, ws_g + kb * NBw + wb0);
+          cp_async_4(slot + 129, ws_g + kb * NBw + wb1);
+        }
+        cp_async_mbar_arrive_noinc(&sfull[sl]);
+        ++q;
+      }
+    }
+    cp_async_wait_all();
   } else if (warp >= kPromoWarp0) {
     // ------------------------------------------------------------ promotion + epilogue
     regs_inc<RegSplit<BN>::kPromo>();
@@ -213,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    const int NBw = Nw / 128;
     uint32_t t = 0;
     bool ok = true;
     for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -221,83 +268,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
       const int row = tl.row0 + quad * 32 + lane;
       const bool valid = row < tl.row1;
-      int tcol0, tcol1, wblk0, wblk1;
+      int tcol0, tcol1, wsel0, wsel1;
       if (FUSE) {
         tcol0 = h * SEG;
         tcol1 = BN / 2 + h * SEG;
-        wblk0 = n0 / 128;
-        wblk1 = (args.N + n0) / 128;
+        wsel0 = 0;  // gate block
+        wsel1 = 1;  // up block
       } else {
         tcol0 = h * (BN / 2);
         tcol1 = h * (BN / 2) + SEG;
-        wblk0 = wblk1 = (n0 + h * (BN / 2)) / 128;
+        wsel0 = wsel1 = (BN == 256) ? h : 0;
       }
-      const float* xs_p = args.xs + (valid ? row : 0);
-      const float* ws_p = args.ws + static_cast<long long>(tl.g) * KB * NBw;
-
-      float acc[2 * SEG];
+      const int rit = quad * 32 + lane;  // row within the tile
+      // fp32 accumulators, kept as pairs for the packed FMA: acc[2i], acc[2i+1]
+      float2 acc[SEG];
 #pragma unroll
-      for (int i = 0; i < 2 * SEG; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < SEG; ++i) acc[i] = make_float2(0.0f, 0.0f);
 
-      float sx_n = valid ? __ldg(xs_p) : 0.0f;
-      float sw0_n = __ldg(ws_p + wblk0), sw1_n = __ldg(ws_p + wblk1);
       for (int kb = 0; kb < KB; ++kb) {
-        const float sx = sx_n, sw0 = sw0_n, sw1 = sw1_n;
-        if (kb + 1 < KB) {
-          sx_n = valid ? __ldg(xs_p + static_cast<long long>(kb + 1) * args.M) : 0.0f;
-          sw0_n = __ldg(ws_p + (kb + 1) * NBw + wblk0);
-          sw1_n = __ldg(ws_p + (kb + 1) * NBw + wblk1);
-        }
         const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
-        const bool got = mbar_wait(&tfull[b], tph, abort_word, lim);
+        const uint32_t sl = t % kScaleSlots, sph = (t / kScaleSlots) & 1u;
+        const bool got = mbar_wait(&tfull[b], tph, abort_word, lim) && mbar_wait(&sfull[sl], sph, abort_word, lim);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
+        const float* slot = scales + sl * kScaleSlotFloats;
+        const float sx = valid ? slot[rit] : 0.0f;
+        const float sw0 = slot[128 + wsel0], sw1 = slot[128 + wsel1];
         tc_fence_after();
         const float f0 = sx * sw0, f1 = sx * sw1;
         const uint32_t tb = t_lane + b * BN;
+        // 32-column chunks: the first SEG/32 belong to segment 0, the rest to
+        // segment 1.  Two TMEM loads are in flight per wait.
+        constexpr int NCH = 2 * SEG / 32, CPS = SEG / 32;
 #pragma unroll
-        for (int cc = 0; cc < SEG / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32(tb + tcol0 + 32 * cc, r);
+        for (int pc = 0; pc < NCH; pc += 2) {
+          uint32_t ra[32], rb[32];
+          const int ca = pc, cb = pc + 1;
+          tmem_ld_32x32(tb + (ca < CPS ? tcol0 + 32 * ca : tcol1 + 32 * (ca - CPS)), ra);
+          tmem_ld_32x32(tb + (cb < CPS ? tcol0 + 32 * cb : tcol1 + 32 * (cb - CPS)), rb);
           tmem_ld_wait();
+          const float2 fa = ca < CPS ? make_float2(f0, f0) : make_float2(f1, f1);
+          const float2 fb = cb < CPS ? make_float2(f0, f0) : make_float2(f1, f1);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[32 * cc + i] = fmaf(__uint_as_float(r[i]), f0, acc[32 * cc + i]);
-        }
+          for (int i = 0; i < 16; ++i)
+            acc[16 * ca + i] =
+                __ffma2_rn(make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), fa,
+                           acc[16 * ca + i]);
 #pragma unroll
-        for (int cc = 0; cc < SEG / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32(tb + tcol1 + 32 * cc, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            acc[SEG + 32 * cc + i] = fmaf(__uint_as_float(r[i]), f1, acc[SEG + 32 * cc + i]);
+          for (int i = 0; i < 16; ++i)
+            acc[16 * cb + i] =
+                __ffma2_rn(make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), fb,
+                           acc[16 * cb + i]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
+        if (lane == 0) {
+          mbar_arrive(&tempty[b]);
+          mbar_arrive(&sempty[sl]);
+        }
         ++t;
       }
       if (!ok) break;
       if (valid) {
         uint16_t* orow = args.out + static_cast<long long>(row) * args.N;
         if (FUSE) {
+          // gate = accumulators [0, SEG), up = [SEG, 2 SEG)
           uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * SEG);
 #pragma unroll
           for (int j = 0; j < SEG; j += 8) {
             float v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = silu_f32(acc[j + i]) * acc[SEG + j + i];
+            for (int i = 0; i < 8; i += 2) {
+              const float2 gt = acc[(j + i) / 2], up = acc[(SEG + j + i) / 2];
+              v[i] = silu_f32(gt.x) * up.x;
+              v[i + 1] = silu_f32(gt.y) * up.y;
+            }
             dst[j / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                                     pack_bf16x2(v[6], v[7]));
           }
         } else {
           uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * (BN / 2));
 #pragma unroll
-          for (int j = 0; j < 2 * SEG; j += 8) {
-            dst[j / 8] = make_uint4(pack_bf16x2(acc[j], acc[j + 1]), pack_bf16x2(acc[j + 2], acc[j + 3]),
-                                    pack_bf16x2(acc[j + 4], acc[j + 5]), pack_bf16x2(acc[j + 6], acc[j + 7]));
+          for (int j = 0; j < SEG; j += 4) {
+            dst[j / 4] = make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                                    pack_bf16x2(acc[j + 2].x, acc[j + 2].y),
+                                    pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
           }
         }
       }

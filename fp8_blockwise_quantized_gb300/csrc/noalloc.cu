@@ -16,7 +16,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/gmm.h"
+#include "gmm.h"
 #include "common.cuh"
 #include "kernels.cuh"
 

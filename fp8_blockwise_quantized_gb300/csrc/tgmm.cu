@@ -13,8 +13,9 @@
 //              belong to the next group (whole 128-byte rows, so the swizzle
 //              does not matter) and fences them into the async proxy; then
 //              tcgen05.mma kind::f16, M=128 (k), N=BN (n), K=16 (rows).
-//   warps 2-9  epilogue: tcgen05.ld -> bf16 -> dW rows; zero tile for an
-//              empty group.
+//   warps 2-9  epilogue: tcgen05.ld -> bf16 -> one shared-memory staging row
+//              per thread -> one bulk async copy per row (256 contiguous
+//              bytes, whole cache lines); zero tile for an empty group.
 // TMEM holds two accumulators, so one tile's epilogue overlaps the next
 // tile's MMAs.  Units are ordered group-major so the tiles of one group (which
 // share its x and dy rows) run together.
@@ -26,7 +27,7 @@ namespace gmm {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kChunk = 64;  // rows per stage
@@ -39,7 +40,11 @@ struct TgmmTile {
   static constexpr int kBBytes = (BN / 64) * kBoxBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  // epilogue staging: one row of BN/2 bf16 per epilogue thread, padded by 16
+  // bytes so a warp's 16-byte stores hit distinct banks
+  static constexpr int kStageRow = BN + 16;
+  static constexpr int kStagingBytes = 2 * kBM * kStageRow;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 };
 
 template <int BN>
@@ -50,7 +55,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint8_t* staging = smem + kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -184,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = pw >> 2;
     const int quad = warp & 3;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    uint8_t* srow = staging + (h * kBM + quad * 32 + lane) * C::kStageRow;
     uint32_t t = 0;
     for (long long u = blockIdx.x; u < num_units; u += gridDim.x) {
       const int g = static_cast<int>(u / (KT * NT));
@@ -191,34 +198,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
       const int r0 = offsets[g], r1 = offsets[g + 1];
       const long long krow = static_cast<long long>(g) * args.K + k0 + quad * 32 + lane;
-      uint4* dst = reinterpret_cast<uint4*>(args.dw + krow * args.N + n0 + h * (BN / 2));
+      uint16_t* dst = args.dw + krow * args.N + n0 + h * (BN / 2);
       if (r1 <= r0) {
+        bulk_wait_read_all();
 #pragma unroll
-        for (int j = 0; j < BN / 16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < BN / 16; ++j) reinterpret_cast<uint4*>(srow)[j] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        bulk_copy_s2g(dst, srow, BN);
+        bulk_commit();
         continue;
       }
       const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, abort_word, lim))) break;
       tc_fence_after();
-      const uint32_t tb = t_lane + b * BN + h * (BN / 2);
+      uint32_t r[BN / 2];
 #pragma unroll
-      for (int cc = 0; cc < BN / 64; ++cc) {
-        uint32_t r[32];
-        tmem_ld_32x32(tb + 32 * cc, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          dst[cc * 4 + j / 8] = make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                           pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                                           pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                                           pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-        }
-      }
+      for (int cc = 0; cc < BN / 64; ++cc)
+        tmem_ld_32x32(t_lane + b * BN + h * (BN / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * cc));
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[b]);
       ++t;
+      bulk_wait_read_all();
+#pragma unroll
+      for (int j = 0; j < BN / 2; j += 8) {
+        reinterpret_cast<uint4*>(srow)[j / 8] =
+            make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                       pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                       pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                       pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+      }
+      fence_proxy_async_smem();
+      bulk_copy_s2g(dst, srow, BN);
+      bulk_commit();
     }
+    bulk_wait_all();
   }
 
   tc_fence_before();
