@@ -20,20 +20,24 @@ namespace gmm {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
 template <int BN, bool FUSE>
 struct Bf16Tile {
+  // plain epilogue: rows staged in shared memory, one bulk copy per row
+  static constexpr bool kStaged = !FUSE;
+  static constexpr int kStages = (kStaged && BN == 256) ? 3 : 4;
+  static constexpr int kStageRow = BN + 16;
+  static constexpr int kStagingBytes = kStaged ? 2 * kBM * kStageRow : 0;
   static constexpr int kABytes = kBM * 64 * 2;   // 16 KB
   static constexpr int kBBytes = 64 * BN * 2;    // BN/64 boxes of 8 KB
   static constexpr int kBoxBytes = 64 * 64 * 2;  // one 64 x 64 bf16 box
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kOutCols = FUSE ? BN / 2 : BN;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 256;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 };
 
 template <int BN, bool FUSE>
@@ -41,10 +45,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     gmm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const FwdArgs args) {
   using C = Bf16Tile<BN, FUSE>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint8_t* staging = smem + kStages * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -204,29 +210,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
       } else {
+        uint32_t r[BN / 2];
 #pragma unroll
-        for (int cc = 0; cc < BN / 64; ++cc) {
-          uint32_t r[32];
-          tmem_ld_32x32(tb + h * (BN / 2) + 32 * cc, r);
-          tmem_ld_wait();
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * (BN / 2) + 32 * cc);
+        for (int cc = 0; cc < BN / 64; ++cc)
+          tmem_ld_32x32(tb + h * (BN / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * cc));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        if (valid) {
+          uint8_t* srow = staging + (h * kBM + quad * 32 + lane) * C::kStageRow;
+          bulk_wait_read_all();
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              dst[j / 8] = make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                      pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                                      pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                                      pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
-            }
+          for (int j = 0; j < BN / 2; j += 8) {
+            reinterpret_cast<uint4*>(srow)[j / 8] =
+                make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                           pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                           pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                           pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
           }
+          fence_proxy_async_smem();
+          bulk_copy_s2g(orow + n0 + h * (BN / 2), srow, BN);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
       ++t;
     }
+    if (C::kStaged) bulk_wait_all();
   }
 
   tc_fence_before();

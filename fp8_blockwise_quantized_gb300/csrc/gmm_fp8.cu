@@ -41,7 +41,6 @@ namespace gmm {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kPromoWarps = 8;
 constexpr int kPromoWarp0 = 4;   // first promotion warp
@@ -61,6 +60,14 @@ constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad
 
 template <int BN, bool FUSE>
 struct Fp8Tile {
+  // The plain (non-fused) epilogue stages each output row in shared memory and
+  // writes it with one bulk copy; its staging takes the room of one ring slot
+  // when BN = 256.  The fused epilogue writes half as many bytes per unit and
+  // stores directly.
+  static constexpr bool kStaged = !FUSE;
+  static constexpr int kStages = (kStaged && BN == 256) ? 3 : 4;
+  static constexpr int kStageRow = BN + 16;  // BN/2 bf16 + 16 bytes of padding
+  static constexpr int kStagingBytes = kStaged ? 2 * kBM * kStageRow : 0;
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -69,7 +76,7 @@ struct Fp8Tile {
   static constexpr int kTmemCols = 2 * BN;             // two partial buffers
   static constexpr int kBarBytes = 512;
   static constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kScaleBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kBarBytes;
 };
 
 template <int BN, bool FUSE>
@@ -78,11 +85,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const FwdArgs args) {
   using C = Fp8Tile<BN, FUSE>;
   constexpr int SEG = C::kSeg;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
-  float* scales = reinterpret_cast<float*>(smem + kStages * C::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes + C::kScaleBytes);
+  uint8_t* staging = smem + kStages * C::kStageBytes;
+  float* scales = reinterpret_cast<float*>(staging + C::kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scales) + C::kScaleBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -349,16 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     pack_bf16x2(v[6], v[7]));
           }
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * (BN / 2));
+          // stage the row (BN/2 bf16 = BN bytes) and write it with one bulk copy
+          uint8_t* srow = staging + (h * kBM + rit) * C::kStageRow;
+          bulk_wait_read_all();
 #pragma unroll
           for (int j = 0; j < SEG; j += 4) {
-            dst[j / 4] = make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
-                                    pack_bf16x2(acc[j + 2].x, acc[j + 2].y),
-                                    pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
+            reinterpret_cast<uint4*>(srow)[j / 4] =
+                make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                           pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
           }
+          fence_proxy_async_smem();
+          bulk_copy_s2g(orow + n0 + h * (BN / 2), srow, BN);
+          bulk_commit();
         }
       }
     }
+    if (C::kStaged) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
