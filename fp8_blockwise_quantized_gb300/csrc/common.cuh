@@ -46,6 +46,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f32(float v) { return v / (1.0f + expf(-v)); }
+// silu(v) = v / (1 + exp(-v)), with the fast hardware exponential and divide
+// (relative error a few ulp of fp32, far below the bf16 rounding that
+// follows).  Saturates correctly: exp(-v) = inf gives 0.
+__device__ __forceinline__ float silu_f32(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+
+// Warp-cooperative store of up to 32 staged rows: row i of the warp lives at
+// stage + i * STRIDE (ROW_BYTES bytes, a multiple of 16) and goes to
+// gdst + i * ld_bytes; rows i >= nvalid are skipped.  Every store
+// instruction writes 512 contiguous bytes per 256-byte pair of rows (or four
+// 128-byte rows), so the output is written in whole cache lines.
+template <int ROW_BYTES, int STRIDE>
+__device__ __forceinline__ void warp_store_rows(const uint8_t* stage, uint8_t* gdst, long long ld_bytes,
+                                                int nvalid, int lane) {
+  constexpr int CPR = ROW_BYTES / 16;  // 16-byte chunks per row
+  static_assert(CPR >= 1 && CPR <= 32 && (32 % CPR) == 0, "row size");
+  constexpr int RPI = 32 / CPR;        // rows per instruction
+  const int c = lane % CPR;
+#pragma unroll
+  for (int it = 0; it < 32 / RPI; ++it) {
+    const int r = it * RPI + lane / CPR;
+    if (r < nvalid)
+      *reinterpret_cast<uint4*>(gdst + r * ld_bytes + c * 16) =
+          *reinterpret_cast<const uint4*>(stage + r * STRIDE + c * 16);
+  }
+}
 
 }  // namespace gmm

@@ -60,14 +60,13 @@ constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad
 
 template <int BN, bool FUSE>
 struct Fp8Tile {
-  // The plain (non-fused) epilogue stages each output row in shared memory and
-  // writes it with one bulk copy; its staging takes the room of one ring slot
-  // when BN = 256.  The fused epilogue writes half as many bytes per unit and
-  // stores directly.
-  static constexpr bool kStaged = !FUSE;
-  static constexpr int kStages = (kStaged && BN == 256) ? 3 : 4;
-  static constexpr int kStageRow = BN + 16;  // BN/2 bf16 + 16 bytes of padding
-  static constexpr int kStagingBytes = kStaged ? 2 * kBM * kStageRow : 0;
+  // The epilogue stages each warp's 32 output rows in shared memory and
+  // writes them with warp-cooperative 512-byte stores.  Its staging takes the
+  // room of one ring slot when BN = 256 (the MMA rarely waits for the ring).
+  static constexpr int kStages = BN == 256 ? 3 : 4;
+  static constexpr int kRowBytes = FUSE ? BN / 4 * 2 : BN;  // bf16 bytes per thread row
+  static constexpr int kStageRow = kRowBytes + 16;         // padded: conflict-free 16-byte stores
+  static constexpr int kStagingBytes = 8 * 32 * kStageRow;
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -340,40 +339,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t;
       }
       if (!ok) break;
-      if (valid) {
-        uint16_t* orow = args.out + static_cast<long long>(row) * args.N;
-        if (FUSE) {
-          // gate = accumulators [0, SEG), up = [SEG, 2 SEG)
-          uint4* dst = reinterpret_cast<uint4*>(orow + n0 + h * SEG);
+      // epilogue: this thread's row -> staging, then the warp stores its rows
+      uint8_t* wstage = staging + pw * 32 * C::kStageRow;
+      uint8_t* srow = wstage + lane * C::kStageRow;
+      if (FUSE) {
+        // gate = accumulators [0, SEG), up = [SEG, 2 SEG)
 #pragma unroll
-          for (int j = 0; j < SEG; j += 8) {
-            float v[8];
+        for (int j = 0; j < SEG; j += 8) {
+          float v[8];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-              const float2 gt = acc[(j + i) / 2], up = acc[(SEG + j + i) / 2];
-              v[i] = silu_f32(gt.x) * up.x;
-              v[i + 1] = silu_f32(gt.y) * up.y;
-            }
-            dst[j / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                    pack_bf16x2(v[6], v[7]));
+          for (int i = 0; i < 8; i += 2) {
+            const float2 gt = acc[(j + i) / 2], up = acc[(SEG + j + i) / 2];
+            v[i] = silu_f32(gt.x) * up.x;
+            v[i + 1] = silu_f32(gt.y) * up.y;
           }
-        } else {
-          // stage the row (BN/2 bf16 = BN bytes) and write it with one bulk copy
-          uint8_t* srow = staging + (h * kBM + rit) * C::kStageRow;
-          bulk_wait_read_all();
+          reinterpret_cast<uint4*>(srow)[j / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
+      } else {
 #pragma unroll
-          for (int j = 0; j < SEG; j += 4) {
-            reinterpret_cast<uint4*>(srow)[j / 4] =
-                make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
-                           pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
-          }
-          fence_proxy_async_smem();
-          bulk_copy_s2g(orow + n0 + h * (BN / 2), srow, BN);
-          bulk_commit();
+        for (int j = 0; j < SEG; j += 4) {
+          reinterpret_cast<uint4*>(srow)[j / 4] =
+              make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
+                         pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
         }
       }
+      __syncwarp();
+      const int wrow0 = tl.row0 + quad * 32;
+      const int nvalid = max(0, min(32, tl.row1 - wrow0));
+      uint16_t* gdst = args.out + static_cast<long long>(wrow0) * args.N + n0 + (FUSE ? h * SEG : h * (BN / 2));
+      warp_store_rows<C::kRowBytes, C::kStageRow>(wstage, reinterpret_cast<uint8_t*>(gdst),
+                                                  static_cast<long long>(args.N) * 2, nvalid, lane);
+      __syncwarp();
     }
-    if (C::kStaged) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
