@@ -4,12 +4,14 @@ The computation lives in the CUDA library ``libgmm_gb300.so`` (C ABI in
 ``include/gmm.h``); this package holds its Python binding, its build script
 and the seeded synthetic workloads.
 """
-from .binding import (EXPORTED, GmmError, LIB_PATH, STATUS_NAMES, Workspace, bf16_fwd, fp8_fwd,
+from .binding import (EXPORTED, GmmError, LIB_PATH, STATUS_NAMES, Workspace, bf16_fwd, dgrad, fp8_fwd,
+                      gmm_bf16_dgrad,
                       gmm_bf16_fwd, gmm_fp8_fwd, gmm_fp8_fwd_noalloc, gmm_get_device_status, gmm_group_metadata,
                       gmm_quantize_lhs, gmm_quantize_rhs, gmm_tiles_offset, gmm_workspace_bytes,
                       group_metadata, load, quantize_lhs, quantize_rhs, tgmm, tgmm_bf16)
 
-__all__ = ["EXPORTED", "GmmError", "LIB_PATH", "STATUS_NAMES", "Workspace", "bf16_fwd", "fp8_fwd",
+__all__ = ["EXPORTED", "GmmError", "LIB_PATH", "STATUS_NAMES", "Workspace", "bf16_fwd", "dgrad", "fp8_fwd",
+           "gmm_bf16_dgrad",
            "gmm_bf16_fwd", "gmm_fp8_fwd", "gmm_fp8_fwd_noalloc", "gmm_get_device_status", "gmm_group_metadata",
            "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_tiles_offset", "gmm_workspace_bytes",
            "group_metadata", "load", "quantize_lhs", "quantize_rhs", "tgmm", "tgmm_bf16"]

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_
 
 EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "gmm_tiles_offset",
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
-            "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc"]
+            "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
+            "gmm_bf16_dgrad"]
 
 
 class GmmError(RuntimeError):
@@ -72,6 +73,8 @@ def load():
     lib.gmm_bf16_fwd.argtypes = [P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.tgmm_bf16.restype = I
     lib.tgmm_bf16.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
+    lib.gmm_bf16_dgrad.restype = I
+    lib.gmm_bf16_dgrad.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
     lib.gmm_get_device_status.restype = I
     lib.gmm_get_device_status.argtypes = [P, P]
     lib.gmm_fp8_fwd_noalloc.restype = I
@@ -135,6 +138,11 @@ def gmm_bf16_fwd(x, w, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, w
                  stream=None) -> int:
     return load().gmm_bf16_fwd(_p(x), _p(w), _p(group_sizes), G, M, K, N, int(fuse_silu_mul),
                                _p(out), _p(workspace), workspace_bytes, _s(stream))
+
+
+def gmm_bf16_dgrad(dy, w, group_sizes, G, M, K, N, dx, workspace, workspace_bytes, stream=None) -> int:
+    return load().gmm_bf16_dgrad(_p(dy), _p(w), _p(group_sizes), G, M, K, N, _p(dx), _p(workspace),
+                                 workspace_bytes, _s(stream))
 
 
 def tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, stream=None) -> int:
@@ -232,6 +240,18 @@ def bf16_fwd(x, w, group_sizes, fuse=False, out=None, workspace=None, stream=Non
     _check(gmm_bf16_fwd(x, w, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes, stream),
            "gmm_bf16_fwd")
     return out
+
+
+def dgrad(dy, w, group_sizes, dx=None, workspace=None, stream=None):
+    """dx [M, K] = dy [M, N] . w[g]^T per group, w [G, K, N]."""
+    M, N = dy.shape
+    G, K, N2 = w.shape
+    assert N2 == N
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    ws_ = _ws(workspace, G, M, dy.device)
+    _check(gmm_bf16_dgrad(dy, w, group_sizes, G, M, K, N, dx, ws_.buf, ws_.nbytes, stream), "gmm_bf16_dgrad")
+    return dx
 
 
 def tgmm(x, dy, group_sizes, dw=None, workspace=None, stream=None):

@@ -284,6 +284,43 @@ gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_bf16 kernel launch");
 }
 
+gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_sizes, int G, int64_t M, int64_t K,
+                          int64_t N, void* dx, void* workspace, size_t workspace_bytes, void* stream) {
+  // dX [M, K] = dY [M, N] . W[g]^T, W [G, K, N]: a grouped GEMM whose
+  // reduction is N and whose output columns are K
+  gmm_status st = check_grouped(G, M, N, K, K);
+  if (st != GMM_OK) return st;
+  if (!w || !group_sizes) return GMM_ERR_NULL;
+  if (M > 0 && (!dy || !dx)) return GMM_ERR_NULL;
+  if (!aligned16(dy) || !aligned16(w) || !aligned16(dx) || !aligned16(group_sizes)) return GMM_ERR_ALIGN;
+  if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != GMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (M == 0) return GMM_OK;
+
+  const int bn = (K % 256 == 0) ? 256 : 128;
+  CUtensorMap map_a, map_b;
+  if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dy, N, M, 64, 128)) != GMM_OK) return st;
+  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, N, static_cast<int64_t>(G) * K, 64, bn)) !=
+      GMM_OK)
+    return st;
+  FwdArgs a{};
+  a.meta = static_cast<const int32_t*>(workspace);
+  a.tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + tiles_offset_bytes(G));
+  a.out = static_cast<uint16_t*>(dx);
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(N);
+  a.N = static_cast<int>(K);
+  a.fuse = 0;
+  a.wait_limit_ns = wait_limit_ns();
+  const long long max_units = tiles_capacity(G, M) * (K / bn);
+  const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
+  cudaError_t e = launch_gmm_bf16_dgrad(map_a, map_b, a, grid, s);
+  return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_bf16 dgrad kernel launch");
+}
+
 gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M, int64_t K,
                      int64_t N, void* dw, void* workspace, size_t workspace_bytes, void* stream) {
   gmm_status st = check_grouped(G, M, K, N, N);

@@ -3,6 +3,11 @@
 // w[g][k,n]) with fp32 accumulation, optionally bf16(silu(gate) * up) with the
 // gate/up weight of "实现差距：GMM Kernel（V1 vs V2）", §3.5.
 //
+// With BK = true the weight operand is K-major instead: the same kernel then
+// computes the bf16 dgrad dX_g = dY_g W[g]^T (the "bwd" phase of "GEMM Kernel
+// 性能优化十问" Q4, bf16 per Q5), with W [G][K][N] read as rows of the output
+// columns, N (its contiguous dimension) being the reduction.
+//
 // Same skeleton as the FP8 kernel without promotion: the accumulator stays in
 // TMEM for the whole K loop (two TMEM buffers so the epilogue of one unit
 // overlaps the MMAs of the next).
@@ -24,7 +29,7 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool BK>
 struct Bf16Tile {
   // plain epilogue: rows staged in shared memory, one bulk copy per row
   static constexpr bool kStaged = !FUSE;
@@ -40,11 +45,12 @@ struct Bf16Tile {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 };
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool BK>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const FwdArgs args) {
-  using C = Bf16Tile<BN, FUSE>;
+  static_assert(!(FUSE && BK), "the fused activation applies to the forward only");
+  using C = Bf16Tile<BN, FUSE, BK>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -104,15 +110,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* a_dst = ring + s * C::kStageBytes;
           uint8_t* b_dst = a_dst + C::kABytes;
-          const int wrow = tl.g * args.K + ks * 64;  // row of the [G*K, Nw] weight view
           mbar_arrive_expect_tx(&full[s], C::kStageBytes);
           tma_load_2d(a_dst, &map_a, &full[s], ks * 64, tl.row0);
+          if (BK) {
+            // K-major weight view [G*N_out, K]: BN rows of output columns
+            tma_load_2d(b_dst, &map_b, &full[s], ks * 64, tl.g * args.N + n0);
+          } else {
+            const int wrow = tl.g * args.K + ks * 64;  // row of the [G*K, Nw] weight view
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i) {
-            int col;
-            if (FUSE) col = (i < BN / 128) ? n0 + 64 * i : args.N + n0 + 64 * (i - BN / 128);
-            else col = n0 + 64 * i;
-            tma_load_2d(b_dst + i * C::kBoxBytes, &map_b, &full[s], col, wrow);
+            for (int i = 0; i < BN / 64; ++i) {
+              int col;
+              if (FUSE) col = (i < BN / 128) ? n0 + 64 * i : args.N + n0 + 64 * (i - BN / 128);
+              else col = n0 + 64 * i;
+              tma_load_2d(b_dst + i * C::kBoxBytes, &map_b, &full[s], col, wrow);
+            }
           }
           ++c;
         }
@@ -127,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(1u /*bf16*/, false, true, kBM, BN);
+      constexpr uint32_t idesc = make_idesc(1u /*bf16*/, false, !BK, kBM, BN);
       uint32_t c = 0, t = 0;
       bool ok = true;
       for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -146,8 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            mma_bf16(d, smem_desc_sw128(a_addr + 32 * j, 16, 1024),
-                     smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024), idesc, (ks > 0 || j > 0) ? 1u : 0u);
+            const uint64_t bdesc = BK ? smem_desc_sw128(b_addr + 32 * j, 16, 1024)
+                                      : smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024);
+            mma_bf16(d, smem_desc_sw128(a_addr + 32 * j, 16, 1024), bdesc, idesc, (ks > 0 || j > 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           ++c;
@@ -252,14 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
 }
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool BK>
 cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                    cudaStream_t stream) {
-  constexpr int smem = Bf16Tile<BN, FUSE>::kSmemBytes;
+  constexpr int smem = Bf16Tile<BN, FUSE, BK>::kSmemBytes;
   cudaError_t e =
-      cudaFuncSetAttribute(gmm_bf16_kernel<BN, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      cudaFuncSetAttribute(gmm_bf16_kernel<BN, FUSE, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gmm_bf16_kernel<BN, FUSE><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
+  gmm_bf16_kernel<BN, FUSE, BK><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
 }
 
@@ -273,9 +285,15 @@ Fp8Geometry bf16_geometry(int N, int fuse) {
 
 cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                             cudaStream_t stream) {
-  if (args.fuse) return launch<256, true>(map_a, map_b, args, grid, stream);
-  if (args.N % 256 == 0) return launch<256, false>(map_a, map_b, args, grid, stream);
-  return launch<128, false>(map_a, map_b, args, grid, stream);
+  if (args.fuse) return launch<256, true, false>(map_a, map_b, args, grid, stream);
+  if (args.N % 256 == 0) return launch<256, false, false>(map_a, map_b, args, grid, stream);
+  return launch<128, false, false>(map_a, map_b, args, grid, stream);
+}
+
+cudaError_t launch_gmm_bf16_dgrad(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
+                                  cudaStream_t stream) {
+  if (args.N % 256 == 0) return launch<256, false, true>(map_a, map_b, args, grid, stream);
+  return launch<128, false, true>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace gmm

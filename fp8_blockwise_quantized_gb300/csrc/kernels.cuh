@@ -42,6 +42,10 @@ cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, c
                            cudaStream_t stream);
 cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                             cudaStream_t stream);
+// bf16 dgrad: the forward kernel with a K-major weight ([G*N_out, K] view);
+// args.K = reduction length, args.N = output columns.
+cudaError_t launch_gmm_bf16_dgrad(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args,
+                                  int grid, cudaStream_t stream);
 cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args,
                              int grid, cudaStream_t stream);
 

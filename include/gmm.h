@@ -141,6 +141,18 @@ gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes
                         size_t workspace_bytes, void* stream);
 
 /*
+ * bf16 dgrad, the activation gradient of the expert GEMM: the "bwd" phase of
+ * "GEMM Kernel 性能优化十问", Q4 (fwd, bwd and tgmm each get their own tiling),
+ * kept in bf16 like the rest of the backward pass (Q5):
+ *   dx[m,k] = bf16( sum_n dy[m,n] * w[g,k,n] ),  m in group g; fp32 accumulation
+ *   dy  bf16 [M, N];  w  bf16 [G, K, N] (the forward weight, natural layout);
+ *   dx  bf16 [M, K]; rows >= S are written as zeros.
+ */
+gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_sizes, int G, int64_t M,
+                          int64_t K, int64_t N, void* dx, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
  * a8 — tgmm, the expert weight gradient ("GEMM Kernel 性能优化十问", Q4:
  * dW[K,N] += X^T[K,M] dY[M,N], M is the reduction; Q5: the backward pass
  * stays bf16, unquantized):

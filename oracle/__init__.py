@@ -79,6 +79,7 @@ def _load():
         lib.oracle_gmm_fp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P]
         lib.oracle_gmm_bf16.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, P]
         lib.oracle_tgmm_bf16.argtypes = [P, P, P, I64, I64, I64, I64, P]
+        lib.oracle_dgrad_bf16.argtypes = [P, P, P, I64, I64, I64, I64, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -238,6 +239,19 @@ def tgmm_bf16(x, dy, group_sizes) -> np.ndarray:
     G = s.size
     out = np.empty((G, K, N), np.float64)
     _check(_load().oracle_tgmm_bf16(_ptr(x), _ptr(dy), _ptr(s), G, M, K, N, _ptr(out)))
+    return out
+
+
+def dgrad_bf16(dy, w, group_sizes) -> np.ndarray:
+    """dx[m, k] = sum_n dy[m, n] * w[g][k, n] (fp64); dy [M, N], w [G, K, N]."""
+    dy = _c(dy, np.uint16)
+    w = _c(w, np.uint16)
+    s = _c(group_sizes, np.int32)
+    M, N = dy.shape
+    G, K, N2 = w.shape
+    assert N2 == N and s.size == G
+    out = np.empty((M, K), np.float64)
+    _check(_load().oracle_dgrad_bf16(_ptr(dy), _ptr(w), _ptr(s), G, M, K, N, _ptr(out)))
     return out
 
 

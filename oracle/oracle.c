@@ -454,6 +454,40 @@ int oracle_tgmm_bf16(const uint16_t *x, const uint16_t *dy, const int32_t *sizes
     return OR_OK;
 }
 
+/* ------------------------------------------------------------------------ */
+/* bf16 dgrad, the activation gradient of the expert GEMM (the "bwd" phase   */
+/* of [Q4], kept in bf16 as [Q5] prescribes for the backward pass):           */
+/*   dx[m,k] = sum_n dy[m,n] * w[g][k,n]      for m in group g                */
+/* rows m >= S are 0.  dy: bf16 [M][N]; w: bf16 [G][K][N]; dx: fp64 [M][K].   */
+/* ------------------------------------------------------------------------ */
+int oracle_dgrad_bf16(const uint16_t *dy, const uint16_t *w, const int32_t *sizes, int64_t G,
+                      int64_t M, int64_t K, int64_t N, double *dx)
+{
+    if (G <= 0 || M < 0 || K <= 0 || N <= 0)
+        return OR_ERR_SHAPE;
+    int64_t *offsets = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G + 1));
+    int st = oracle_group_offsets(sizes, G, M, offsets);
+    if (st != OR_OK) {
+        free(offsets);
+        return st;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t g = group_of_row(offsets, G, m);
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            if (g >= 0) {
+                const uint16_t *wrow = w + (g * K + k) * N;
+                for (int64_t n = 0; n < N; ++n)
+                    acc += (double)bf16_bits_to_float(dy[m * N + n]) * (double)bf16_bits_to_float(wrow[n]);
+            }
+            dx[m * K + k] = acc;
+        }
+    }
+    free(offsets);
+    return OR_OK;
+}
+
 /* Number of OpenMP threads the oracle runs with (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -319,3 +319,20 @@ def test_tgmm_tiny_brute_force():
     assert dw[0, 0, 5] == 1 * 4 + 2 * -1
     assert dw[1, 0, 5] == 3 * 0.5
     assert np.count_nonzero(dw) == 2
+
+
+def test_dgrad_equals_library_and_transposed_forward():
+    # dX_g = dY_g W[g]^T: a library matmul per group, and the bf16 forward GMM
+    # of dY with the transposed weights (a different oracle routine)
+    rng = _rng(24)
+    G, K, N = 3, 256, 384
+    sizes = np.array([20, 0, 33], np.int32)
+    M = 60
+    dy = _bf16(rng.standard_normal((M, N)))
+    w = _bf16(rng.standard_normal((G, K, N)) / 8)
+    dx = oracle.dgrad_bf16(dy, w, sizes)
+    wt = np.ascontiguousarray(w.transpose(0, 2, 1))
+    ref = _torch_group_mm(bf16_bits_to_f32(dy).astype(np.float64), bf16_bits_to_f32(wt).astype(np.float64), sizes)
+    np.testing.assert_allclose(dx, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(dx, oracle.gmm_bf16(dy, wt, sizes))
+    assert np.all(dx[53:] == 0)
