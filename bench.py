@@ -4,11 +4,11 @@ One step = one pass of the whole path over the production-shape MoE expert
 layer ("GEMM Kernel 性能优化十问", Q6: G=256 experts, M = 2 x 4096 x top-8 =
 65536 rows, K = 2048, N = 512):
     1. dynamic 1x128 FP8 quantization of X              (gmm_quantize_lhs)
-    2. wi: FP8 blockwise GMM, fused silu(gate)*up -> h  (gmm_fp8_fwd, 2N cols)
-    3. 1x128 FP8 quantization of h                      (gmm_quantize_lhs)
-    4. wo: FP8 blockwise GMM -> y                       (gmm_fp8_fwd)
-    5. wo weight gradient  dW_wo[g] = h_g^T dY_g         (tgmm_bf16)
-    6. wi weight gradient  dW_wi[g] = X_g^T dH_g         (tgmm_bf16)
+    2. wi: FP8 blockwise GMM, fused silu(gate)*up -> h, with the 1x128 FP8
+       quantization of h fused into its epilogue         (gmm_fp8_fwd_swiglu_quant)
+    3. wo: FP8 blockwise GMM on the quantized h -> y     (gmm_fp8_fwd)
+    4. wo weight gradient  dW_wo[g] = h_g^T dY_g         (tgmm_bf16)
+    5. wi weight gradient  dW_wi[g] = X_g^T dH_g         (tgmm_bf16)
 each grouped call running its own device metadata kernel.  The metric is
 TFLOP/s counted as 2*M*K*N per GMM (FLOPs do not depend on precision, Q7),
 summed over the four GMMs.  Weights are quantized once, offline, before
@@ -42,7 +42,7 @@ if ROOT not in sys.path:
 METRIC = "FP8 GMM fwd & bf16 tgmm TFLOPS (2MKN)"
 UNIT = "TFLOP/s"
 WORKLOAD = ("production MoE expert layer, G=256 M=65536 (8192 tokens x top-8, Zipf(1.1) routing, "
-            "8 empty experts): quantize X, FP8 wi K=2048 N=2x512 fused silu*up, quantize h, "
+            "8 empty experts): quantize X, FP8 wi K=2048 N=2x512 fused silu*up + FP8 cast of h, "
             "FP8 wo K=512 N=2048, bf16 tgmm dW_wo and dW_wi")
 G, M, K, N = 256, 65536, 2048, 512
 FALLBACK_HBM_GBS = 6800.0
@@ -138,12 +138,10 @@ def accounting(sizes: np.ndarray):
     # quantize X: read bf16, write e4m3 + fp32 scale per 128
     b["quantize_x"] = M * K * 2 + M * K + M * K // 128 * 4
     f["quantize_x"] = 0
-    # wi fused: Xq, xs, live experts' Wq/ws, h out
+    # wi fused: Xq, xs, live experts' Wq/ws in; h (bf16), hq (e4m3), hs (fp32) out
     f["gmm_fp8_wi"] = 2 * Mr * K * 2 * N
     b["gmm_fp8_wi"] = M * K + M * (K // 128) * 4 + live * K * 2 * N + live * (K // 128) * (2 * N // 128) * 4 \
-        + M * N * 2 + 4 * G
-    b["quantize_h"] = M * N * 2 + M * N + M * N // 128 * 4
-    f["quantize_h"] = 0
+        + M * N * 2 + M * N + M * (N // 128) * 4 + 4 * G
     f["gmm_fp8_wo"] = 2 * Mr * N * K
     b["gmm_fp8_wo"] = M * N + M * (N // 128) * 4 + live * N * K + live * (N // 128) * (K // 128) * 4 \
         + M * K * 2 + 4 * G
@@ -177,7 +175,7 @@ def _traffic(kernel):
     return t["bytes"] if h == t["sha256"] else None
 
 
-KERNEL_KIND = {"quantize_x": "hbm", "quantize_h": "hbm", "gmm_fp8_wi": "fp8", "gmm_fp8_wo": "fp8",
+KERNEL_KIND = {"quantize_x": "hbm", "gmm_fp8_wi": "fp8", "gmm_fp8_wo": "fp8",
                "tgmm_wo": "bf16", "tgmm_wi": "bf16"}
 
 
@@ -242,7 +240,7 @@ def run_gpu(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     chk = gmm.binding._check
 
-    names = ["quantize_x", "gmm_fp8_wi", "quantize_h", "gmm_fp8_wo", "tgmm_wo", "tgmm_wi"]
+    names = ["quantize_x", "gmm_fp8_wi", "gmm_fp8_wo", "tgmm_wo", "tgmm_wi"]
 
     def step(ev=None):
         def mark(i):
@@ -251,21 +249,20 @@ def run_gpu(args):
         mark(0)
         chk(gmm.gmm_quantize_lhs(x, M, K, xq, xs, stream), "quantize X")
         mark(1)
-        chk(gmm.gmm_fp8_fwd(xq, xs, wq_wi, ws_wi, sizes, G, M, K, N, 1, h, work.buf, work.nbytes,
-                            stream), "wi")
+        chk(gmm.gmm_fp8_fwd_swiglu_quant(xq, xs, wq_wi, ws_wi, sizes, G, M, K, N, h, hq, hs, work.buf,
+                                         work.nbytes, stream), "wi")
         mark(2)
-        chk(gmm.gmm_quantize_lhs(h, M, N, hq, hs, stream), "quantize h")
-        mark(3)
         chk(gmm.gmm_fp8_fwd(hq, hs, wq_wo, ws_wo, sizes, G, M, N, K, 0, y, work.buf, work.nbytes,
                             stream), "wo")
-        mark(4)
+        mark(3)
         chk(gmm.tgmm_bf16(h, dy, sizes, G, M, N, K, dw_wo, work.buf, work.nbytes, stream), "tgmm wo")
-        mark(5)
+        mark(4)
         chk(gmm.tgmm_bf16(x, dh, sizes, G, M, K, 2 * N, dw_wi, work.buf, work.nbytes, stream),
             "tgmm wi")
-        mark(6)
+        mark(5)
 
-    launches_per_step = 10  # 2 quantize + 4 metadata + 2 fp8 GMM + 2 tgmm
+    n_marks = len(names) + 1
+    launches_per_step = 9  # 1 quantize + 4 metadata + 2 fp8 GMM + 2 tgmm
 
     for _ in range(args.warmup):
         step()
@@ -274,7 +271,7 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError(f"device status {gmm.STATUS_NAMES.get(st, st)} after warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(args.steps)]
     clocks = Clocks(dev.index if dev.index is not None else 0)
     clocks.start()
     # keep the GPU busy while the sampler starts (its first sample takes ~0.1 s)
@@ -301,7 +298,7 @@ def run_gpu(args):
     per_kernel = {n: [] for n in names}
     step_ms = []
     for ev in events:
-        step_ms.append(ev[0].elapsed_time(ev[6]))
+        step_ms.append(ev[0].elapsed_time(ev[n_marks - 1]))
         for j, n in enumerate(names):
             per_kernel[n].append(ev[j].elapsed_time(ev[j + 1]))
     ms = float(np.mean(step_ms))
@@ -360,7 +357,7 @@ def run_gpu(args):
         wi_ms = float(np.mean([a for a, _ in tb]))
         wo_ms = float(np.mean([b for _, b in tb]))
         fp8_ms = kern["gmm_fp8_wi"]["ms"] + kern["gmm_fp8_wo"]["ms"]
-        q_ms = kern["quantize_x"]["ms"] + kern["quantize_h"]["ms"]
+        q_ms = kern["quantize_x"]["ms"]
         bf = {"wi_ms": round(wi_ms, 4), "wo_ms": round(wo_ms, 4),
               "wi_TFLOP/s": round(flops["gmm_fp8_wi"] / (wi_ms * 1e-3) / 1e12, 1),
               "wo_TFLOP/s": round(flops["gmm_fp8_wo"] / (wo_ms * 1e-3) / 1e12, 1),
@@ -384,9 +381,8 @@ def run_gpu(args):
             dy_d.copy_(dy_h, non_blocking=True)
             dh_d.copy_(dh_h, non_blocking=True)
             chk(gmm.gmm_quantize_lhs(x_d, M, K, xq, xs, stream), "e2e quantize X")
-            chk(gmm.gmm_fp8_fwd(xq, xs, wq_wi, ws_wi, s_d, G, M, K, N, 1, h, work.buf, work.nbytes, stream),
-                "e2e wi")
-            chk(gmm.gmm_quantize_lhs(h, M, N, hq, hs, stream), "e2e quantize h")
+            chk(gmm.gmm_fp8_fwd_swiglu_quant(xq, xs, wq_wi, ws_wi, s_d, G, M, K, N, h, hq, hs, work.buf,
+                                             work.nbytes, stream), "e2e wi")
             chk(gmm.gmm_fp8_fwd(hq, hs, wq_wo, ws_wo, s_d, G, M, N, K, 0, y, work.buf, work.nbytes, stream),
                 "e2e wo")
             chk(gmm.tgmm_bf16(h, dy_d, s_d, G, M, N, K, dw_wo, work.buf, work.nbytes, stream), "e2e tgmm wo")
@@ -552,18 +548,24 @@ def run_profile_case(args):
     def bf16(shape, std=1.0):
         return (torch.randn(shape, generator=gen, device=dev) * std).to(torch.bfloat16)
 
-    if case in ("fp8_wi", "fp8_wo"):
-        k, n, fuse = (K, N, 1) if case == "fp8_wi" else (N, K, 0)
+    if case in ("fp8_wi", "fp8_wo", "fp8_wi_quant"):
+        k, n, fuse = (K, N, 1) if case != "fp8_wo" else (N, K, 0)
         x = bf16((M, k))
         xq, xs = gmm.quantize_lhs(x)
         w = bf16((G, k, 2 * n if fuse else n), 1.0 / math.sqrt(k))
         wq, ws = gmm.quantize_rhs(w)
         del x, w
         out = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        hq = torch.empty((M, n), dtype=torch.uint8, device=dev)
+        hs = torch.empty((n // 128, M), dtype=torch.float32, device=dev)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        run = lambda: chk(gmm.gmm_fp8_fwd(xq, xs, wq, ws, sizes, G, M, k, n, fuse, out, work.buf,
-                                          work.nbytes, None), case)
+        if case == "fp8_wi_quant":
+            run = lambda: chk(gmm.gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, sizes, G, M, k, n, out, hq, hs,
+                                                           work.buf, work.nbytes, None), case)
+        else:
+            run = lambda: chk(gmm.gmm_fp8_fwd(xq, xs, wq, ws, sizes, G, M, k, n, fuse, out, work.buf,
+                                              work.nbytes, None), case)
     elif case in ("tgmm_wi", "tgmm_wo"):
         k, n = (K, 2 * N) if case == "tgmm_wi" else (N, K)
         x = bf16((M, k))
@@ -597,7 +599,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bf16-baseline", action="store_true")
     ap.add_argument("--profile-case", default=None,
-                    choices=["fp8_wi", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
+                    choices=["fp8_wi", "fp8_wi_quant", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
                     help="run one kernel at the production shape (for ncu) and exit")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured for this build")

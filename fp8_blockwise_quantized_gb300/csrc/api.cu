@@ -248,6 +248,48 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 kernel launch");
 }
 
+gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq, const float* ws,
+                                    const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
+                                    void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream) {
+  const int64_t Nw = 2 * N;
+  gmm_status st = check_grouped(G, M, K, N, Nw);
+  if (st != GMM_OK) return st;
+  if (!wq || !ws || !group_sizes) return GMM_ERR_NULL;
+  if (M > 0 && (!xq || !xs || !hq || !hs)) return GMM_ERR_NULL;
+  if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(h) || !aligned16(hq) ||
+      !aligned16(hs) || !aligned16(group_sizes))
+    return GMM_ERR_ALIGN;
+  if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != GMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (M == 0) return GMM_OK;
+
+  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), 1);
+  CUtensorMap map_a, map_b;
+  if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
+  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
+    return st;
+  FwdArgs a{};
+  a.xs = xs;
+  a.ws = ws;
+  a.meta = static_cast<const int32_t*>(workspace);
+  a.tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + tiles_offset_bytes(G));
+  a.out = static_cast<uint16_t*>(h);
+  a.hq = static_cast<uint8_t*>(hq);
+  a.hs = hs;
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.fuse = 1;
+  a.wait_limit_ns = wait_limit_ns();
+  const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
+  const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
+  cudaError_t e = launch_gmm_fp8(map_a, map_b, a, grid, s);
+  return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 fused-quant kernel launch");
+}
+
 gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes, int G, int64_t M, int64_t K,
                         int64_t N, int fuse_silu_mul, void* out, void* workspace, size_t workspace_bytes,
                         void* stream) {

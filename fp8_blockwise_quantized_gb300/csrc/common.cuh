@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 namespace gmm {
@@ -44,6 +45,20 @@ struct Tile {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Per-block quantization arithmetic ("实现差距：GMM Kernel（V1 vs V2）", §3.3):
+// scale = absmax / 448 and inv = (scale == 0 ? 0 : 1 / scale), both IEEE fp32
+// round-to-nearest divisions; codes = e4m3(x * inv), nearest-even, saturating.
+// Shared by the quantize kernels and the fused epilogue so that both produce
+// the same bits.
+__device__ __forceinline__ void e4m3_block_scale(float absmax, float& s, float& inv) {
+  s = __fdiv_rn(absmax, 448.0f);
+  inv = (s == 0.0f) ? 0.0f : __fdiv_rn(1.0f, s);
+}
+// 2 x fp32 -> 2 x e4m3; `lo` is the lower byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
 // silu(v) = v / (1 + exp(-v)), with the fast hardware exponential and divide

@@ -58,7 +58,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kScaleSlots = 8;        // K blocks of scales in flight
 constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool QUANT>
 struct Fp8Tile {
   // The epilogue stages each warp's 32 output rows in shared memory and
   // writes them with warp-cooperative 512-byte stores.  Its staging takes the
@@ -75,14 +75,19 @@ struct Fp8Tile {
   static constexpr int kTmemCols = 2 * BN;             // two partial buffers
   static constexpr int kBarBytes = 512;
   static constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kBarBytes;
+  // fused quantized output: the two column halves of a row's 1x128 block meet
+  // through a double-buffered absmax exchange
+  static constexpr int kExchangeBytes = QUANT ? 2 * 2 * kBM * 4 : 0;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kExchangeBytes + kBarBytes;
 };
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const FwdArgs args) {
-  using C = Fp8Tile<BN, FUSE>;
+  static_assert(!QUANT || (FUSE && BN == 256), "the quantized output is for the fused 128-column units");
+  using C = Fp8Tile<BN, FUSE, QUANT>;
   constexpr int SEG = C::kSeg;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -90,13 +95,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   uint8_t* staging = smem + kStages * C::kStageBytes;
   float* scales = reinterpret_cast<float*>(staging + C::kStagingBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scales) + C::kScaleBytes);
+  float* amax_x = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scales) + C::kScaleBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(amax_x) + C::kExchangeBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kScaleSlots;
-  uint64_t* drain = sempty + kScaleSlots;
+  uint64_t* ebar = sempty + kScaleSlots;  // absmax exchange of the fused quantized output
+  uint64_t* drain = ebar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sfull[q], 32);  // one cp.async arrival per loader lane
       mbar_init(&sempty[q], kPromoWarps);
     }
+    mbar_init(ebar, kPromoWarps);
     mbar_init(drain, 1);
     *abort_word = 0;
     fence_mbar_init();
@@ -262,14 +270,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long total = static_cast<long long>(args.M - S) * args.N / 8;
         uint4* p = reinterpret_cast<uint4*>(args.out + static_cast<long long>(S) * args.N);
         const long long stride = static_cast<long long>(gridDim.x) * (kPromoWarps * 32);
-        for (long long i = static_cast<long long>(blockIdx.x) * (kPromoWarps * 32) + (threadIdx.x - kPromoWarp0 * 32);
-             i < total;
-             i += stride)
-          p[i] = make_uint4(0, 0, 0, 0);
+        const long long tid = static_cast<long long>(blockIdx.x) * (kPromoWarps * 32) + (threadIdx.x - kPromoWarp0 * 32);
+        if (args.out)
+          for (long long i = tid; i < total; i += stride) p[i] = make_uint4(0, 0, 0, 0);
+        if (QUANT) {
+          // codes 0 and scale 0, as quantizing the zero rows gives
+          uint4* q = reinterpret_cast<uint4*>(args.hq + static_cast<long long>(S) * args.N);
+          for (long long i = tid; i < total / 2; i += stride) q[i] = make_uint4(0, 0, 0, 0);
+          const long long rows = args.M - S;
+          for (long long i = tid; i < rows * (args.N / 128); i += stride)
+            args.hs[(i / rows) * args.M + S + (i % rows)] = 0.0f;
+        }
       }
     }
 
-    uint32_t t = 0;
+    uint32_t t = 0, ue = 0;
     bool ok = true;
     for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const Tile tl = args.tiles[u / units_per_tile];
@@ -343,18 +358,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* wstage = staging + pw * 32 * C::kStageRow;
       uint8_t* srow = wstage + lane * C::kStageRow;
       if (FUSE) {
-        // gate = accumulators [0, SEG), up = [SEG, 2 SEG)
+        // gate = accumulators [0, SEG), up = [SEG, 2 SEG); h = bf16(silu(gate) * up)
+        uint32_t hb[SEG / 2];
+        float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < SEG; j += 8) {
-          float v[8];
+        for (int j = 0; j < SEG; j += 2) {
+          const float2 gt = acc[j / 2], up = acc[(SEG + j) / 2];
+          hb[j / 2] = pack_bf16x2(silu_f32(gt.x) * up.x, silu_f32(gt.y) * up.y);
+          if (QUANT)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb[j / 2] << 16)),
+                                     fabsf(__uint_as_float(hb[j / 2] & 0xffff0000u))));
+        }
 #pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const float2 gt = acc[(j + i) / 2], up = acc[(SEG + j + i) / 2];
-            v[i] = silu_f32(gt.x) * up.x;
-            v[i + 1] = silu_f32(gt.y) * up.y;
+        for (int j = 0; j < SEG / 8; ++j)
+          reinterpret_cast<uint4*>(srow)[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
+        if (QUANT) {
+          // the 1x128 block of this row spans both column halves (two warpgroups):
+          // exchange the halves' absmax, then quantize the bf16 values exactly as
+          // gmm_quantize_lhs would
+          float* ex = amax_x + (ue & 1u) * (2 * kBM);
+          ex[h * kBM + rit] = amax;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ebar);
+          if (!__all_sync(0xffffffffu, mbar_wait(ebar, ue & 1u, abort_word, lim))) break;
+          ++ue;
+          float sc, inv;
+          e4m3_block_scale(fmaxf(ex[rit], ex[kBM + rit]), sc, inv);
+          if (valid) {
+            uint4* qdst = reinterpret_cast<uint4*>(args.hq + static_cast<long long>(row) * args.N + n0 + h * SEG);
+#pragma unroll
+            for (int j = 0; j < SEG / 16; ++j) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t p0 = hb[8 * j + 2 * i], p1 = hb[8 * j + 2 * i + 1];
+                w[i] = e4m3x2(__fmul_rn(__uint_as_float(p0 << 16), inv),
+                              __fmul_rn(__uint_as_float(p0 & 0xffff0000u), inv)) |
+                       (e4m3x2(__fmul_rn(__uint_as_float(p1 << 16), inv),
+                               __fmul_rn(__uint_as_float(p1 & 0xffff0000u), inv))
+                        << 16);
+              }
+              qdst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            if (h == 0) args.hs[static_cast<long long>(n0 / 128) * args.M + row] = sc;
           }
-          reinterpret_cast<uint4*>(srow)[j / 8] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
         }
       } else {
 #pragma unroll
@@ -366,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       const int wrow0 = tl.row0 + quad * 32;
-      const int nvalid = max(0, min(32, tl.row1 - wrow0));
+      const int nvalid = args.out ? max(0, min(32, tl.row1 - wrow0)) : 0;
       uint16_t* gdst = args.out + static_cast<long long>(wrow0) * args.N + n0 + (FUSE ? h * SEG : h * (BN / 2));
       warp_store_rows<C::kRowBytes, C::kStageRow>(wstage, reinterpret_cast<uint8_t*>(gdst),
                                                   static_cast<long long>(args.N) * 2, nvalid, lane);
@@ -384,13 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
 }
 
-template <int BN, bool FUSE>
+template <int BN, bool FUSE, bool QUANT>
 cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                    cudaStream_t stream) {
-  constexpr int smem = Fp8Tile<BN, FUSE>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(gmm_fp8_kernel<BN, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = Fp8Tile<BN, FUSE, QUANT>::kSmemBytes;
+  cudaError_t e =
+      cudaFuncSetAttribute(gmm_fp8_kernel<BN, FUSE, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gmm_fp8_kernel<BN, FUSE><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
+  gmm_fp8_kernel<BN, FUSE, QUANT><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
   return cudaGetLastError();
 }
 
@@ -404,9 +452,10 @@ Fp8Geometry fp8_geometry(int N, int fuse) {
 
 cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                            cudaStream_t stream) {
-  if (args.fuse) return launch<256, true>(map_a, map_b, args, grid, stream);
-  if (args.N % 256 == 0) return launch<256, false>(map_a, map_b, args, grid, stream);
-  return launch<128, false>(map_a, map_b, args, grid, stream);
+  if (args.fuse && args.hq) return launch<256, true, true>(map_a, map_b, args, grid, stream);
+  if (args.fuse) return launch<256, true, false>(map_a, map_b, args, grid, stream);
+  if (args.N % 256 == 0) return launch<256, false, false>(map_a, map_b, args, grid, stream);
+  return launch<128, false, false>(map_a, map_b, args, grid, stream);
 }
 
 }  // namespace gmm

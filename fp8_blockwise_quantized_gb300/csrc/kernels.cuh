@@ -24,7 +24,9 @@ struct FwdArgs {
   const float* ws;        // fp32 [G][K/128][Nw/128] (FP8 only)
   const int32_t* meta;    // workspace words
   const Tile* tiles;      // workspace tile list
-  uint16_t* out;          // bf16 [M][N]
+  uint16_t* out;          // bf16 [M][N] (may be null with hq)
+  uint8_t* hq;            // fused quantized output: e4m3 [M][N] (null: none)
+  float* hs;              // fused quantized output scales: fp32 [N/128][M]
   int M, K, N;            // N = output columns
   int fuse;               // 1: silu(gate) * up, W has 2N columns
   uint64_t wait_limit_ns;

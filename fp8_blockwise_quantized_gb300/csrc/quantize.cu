@@ -8,24 +8,12 @@
 // The scale arithmetic is IEEE fp32 with round-to-nearest: __fdiv_rn and
 // __fmul_rn keep the compiler from contracting or approximating it, so the
 // codes and scales are bit-identical to any correct fp32 implementation.
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace gmm {
 
 namespace {
-
-__device__ __forceinline__ void block_scale(float absmax, float& s, float& inv) {
-  s = __fdiv_rn(absmax, 448.0f);
-  inv = (s == 0.0f) ? 0.0f : __fdiv_rn(1.0f, s);
-}
-
-// 2 x fp32 -> 2 x e4m3 (nearest even, saturating); `lo` is the lower byte.
-__device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
-}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -70,12 +58,12 @@ __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restri
 #pragma unroll
       for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
       float s, inv;
-      block_scale(amax, s, inv);
+      e4m3_block_scale(amax, s, inv);
       uint2 q;
-      q.x = to_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-            (to_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
-      q.y = to_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-            (to_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
+      q.x = e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
+            (e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
+      q.y = e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
+            (e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
       if (b < nblocks) {
         xq[b * 16 + l16] = q;
         if (l16 == 0) {
@@ -123,10 +111,10 @@ __global__ void __launch_bounds__(256) quantize_rhs_kernel(const uint16_t* __res
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
   float s, inv;
-  block_scale(amax, s, inv);
+  e4m3_block_scale(amax, s, inv);
 #pragma unroll
   for (int j = 0; j < 64; j += 2) {
-    const uint32_t q = to_e4m3x2(__fmul_rn(f[j], inv), __fmul_rn(f[j + 1], inv));
+    const uint32_t q = e4m3x2(__fmul_rn(f[j], inv), __fmul_rn(f[j + 1], inv));
     tile[c0 + j][kr] = static_cast<uint8_t>(q & 0xff);
     tile[c0 + j + 1][kr] = static_cast<uint8_t>(q >> 8);
   }

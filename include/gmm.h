@@ -129,6 +129,21 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
                        void* stream);
 
 /*
+ * FP8 forward of the gate/up layer with the next layer's quantization fused
+ * into its epilogue: "MoE 优化的探索" §5.1 names the step between Linear-1 and
+ * Linear-2 "SwiGLU / FP8 Cast"; here the wi kernel emits, besides (optionally)
+ * h = bf16(silu(gate) * up), its 1x128 e4m3 quantization directly:
+ *   hq, hs  = exactly what gmm_quantize_lhs(h, M, N, hq, hs) would write
+ *             (the absmax is taken over the bf16-rounded h; same fp32 arithmetic)
+ * Arguments as gmm_fp8_fwd with fuse_silu_mul = 1 (wq holds 2N columns), plus
+ *   h   bf16 [M, N] or NULL (then only hq, hs are written)
+ *   hq  e4m3 [M, N];  hs  fp32 [N/128, M]; rows >= S get codes 0 and scale 0.
+ */
+gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq, const float* ws,
+                                    const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
+                                    void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * a7 — bf16 GMM forward, unquantized (the BF16 baseline of "GEMM Kernel
  * 性能优化十问", Q7/Q10 step 4): out[m,n] = bf16(sum_k x[m,k] * w[g,k,n]),
  * fp32 accumulation; fuse_silu_mul as for gmm_fp8_fwd.
