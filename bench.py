@@ -119,6 +119,25 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job's time).
+    Works on any torch.distributed backend (NCCL with a CUDA device, gloo on
+    the CPU); a single process returns the value unchanged."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_step: float, steps: int, total_ms_max: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of the same (replicated)
+    workload; the job took as long as its slowest rank."""
+    return world * flops_per_step * steps / (total_ms_max * 1e-3) / 1e12
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -304,12 +323,10 @@ def run_gpu(args):
     ms = float(np.mean(step_ms))
     total_ms = float(np.sum(step_ms))
     if ws_ > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dev)
         ms = total_ms / args.steps
     step_flops = sum(flops.values())
-    value = ws_ * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(ws_, step_flops, args.steps, total_ms)
 
     peaks = _peaks()
     fp8_peak = 2.0 * peaks["bf16"]
@@ -401,9 +418,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1) / n_e2e
         if ws_ > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+            e_ms = max_over_ranks(e_ms, dev)
         h2d = x.numel() * 2 + dy.numel() * 2 + dh.numel() * 2 + sizes.numel() * 4
         d2h = y.numel() * 2
         e2e = {"value": round(ws_ * step_flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,

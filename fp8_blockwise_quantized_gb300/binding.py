@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_
 EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "gmm_tiles_offset",
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
             "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
-            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant"]
+            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout"]
 
 
 class GmmError(RuntimeError):
@@ -79,6 +79,8 @@ def load():
     lib.gmm_bf16_dgrad.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
     lib.gmm_get_device_status.restype = I
     lib.gmm_get_device_status.argtypes = [P, P]
+    lib.gmm_selftest_wait_timeout.restype = I
+    lib.gmm_selftest_wait_timeout.argtypes = [P, SZ, I, P]
     lib.gmm_fp8_fwd_noalloc.restype = I
     lib.gmm_fp8_fwd_noalloc.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P]
     _lib = lib
@@ -160,6 +162,10 @@ def tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, st
 
 def gmm_get_device_status(workspace, stream=None) -> int:
     return load().gmm_get_device_status(_p(workspace), _s(stream))
+
+
+def gmm_selftest_wait_timeout(workspace, workspace_bytes, limit_ms, stream=None) -> int:
+    return load().gmm_selftest_wait_timeout(_p(workspace), workspace_bytes, int(limit_ms), _s(stream))
 
 
 def gmm_fp8_fwd_noalloc(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out,

@@ -380,9 +380,13 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
   // reads x or dy, so the maps may describe a dummy one-row tensor.
   const void* xb = M > 0 ? x : dw;
   const void* db = M > 0 ? dy : dw;
-  CUtensorMap map_x, map_dy;
+  CUtensorMap map_x, map_dy, map_dw;
   if ((st = encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, K, M, 64, 64)) != GMM_OK) return st;
   if ((st = encode_2d(&map_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, db, N, M, 64, 64)) != GMM_OK) return st;
+  // dW viewed as [G*K, N], written in 32-row x 64-column boxes
+  if ((st = encode_2d(&map_dw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dw, N, static_cast<int64_t>(G) * K, 64, 32)) !=
+      GMM_OK)
+    return st;
   TgmmArgs a{};
   a.meta = static_cast<const int32_t*>(workspace);
   a.dw = static_cast<uint16_t*>(dw);
@@ -393,7 +397,7 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
   a.wait_limit_ns = wait_limit_ns();
   const long long units = static_cast<long long>(G) * (K / 128) * (N / tgmm_bn(static_cast<int>(N)));
   const int grid = static_cast<int>(units < di.sms ? units : di.sms);
-  cudaError_t e = launch_tgmm_bf16(map_x, map_dy, a, grid, s);
+  cudaError_t e = launch_tgmm_bf16(map_x, map_dy, map_dw, a, grid, s);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "tgmm kernel launch");
 }
 

@@ -48,8 +48,8 @@ cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, 
 // args.K = reduction length, args.N = output columns.
 cudaError_t launch_gmm_bf16_dgrad(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args,
                                   int grid, cudaStream_t stream);
-cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args,
-                             int grid, cudaStream_t stream);
+cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
+                             const TgmmArgs& args, int grid, cudaStream_t stream);
 
 // Tile geometry the host needs to build tensor maps and size grids.
 struct Fp8Geometry {

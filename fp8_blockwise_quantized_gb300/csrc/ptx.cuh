@@ -118,6 +118,15 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Wait until this thread's committed bulk copies have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Tiled tensor store shared -> global (one box of the tensor map), tracked in
+// this thread's bulk async-group.  x, y >= 0, x aligned as for loads.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (the tensor core and the bulk-copy engine read through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {

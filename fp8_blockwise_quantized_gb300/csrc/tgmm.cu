@@ -13,9 +13,10 @@
 //              belong to the next group (whole 128-byte rows, so the swizzle
 //              does not matter) and fences them into the async proxy; then
 //              tcgen05.mma kind::f16, M=128 (k), N=BN (n), K=16 (rows).
-//   warps 2-9  epilogue: tcgen05.ld -> bf16 -> one shared-memory staging row
-//              per thread -> one bulk async copy per row (256 contiguous
-//              bytes, whole cache lines); zero tile for an empty group.
+//   warps 2-9  epilogue: tcgen05.ld -> bf16 -> the warp's 32 rows staged in
+//              shared memory one 32x64 box at a time (128-byte swizzle) -> one
+//              TMA tensor store per box; zero tile for an empty group.  The
+//              small staging area leaves room for a 4-slot load ring.
 // TMEM holds two accumulators, so one tile's epilogue overlaps the next
 // tile's MMAs.  Units are ordered group-major so the tiles of one group (which
 // share its x and dy rows) run together.
@@ -27,7 +28,7 @@ namespace gmm {
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kChunk = 64;  // rows per stage
@@ -42,14 +43,15 @@ struct TgmmTile {
   static constexpr int kTmemCols = 2 * BN;
   // epilogue staging: one row of BN/2 bf16 per epilogue thread, padded by 16
   // bytes so a warp's 16-byte stores hit distinct banks
-  static constexpr int kStageRow = BN + 16;
-  static constexpr int kStagingBytes = 2 * kBM * kStageRow;
+  // one 32-row x 64-column bf16 box (4 KB) per epilogue warp
+  static constexpr int kStagingBytes = kEpiWarps * 4096;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 };
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tgmm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dy,
+                const __grid_constant__ CUtensorMap map_dw,
                 const TgmmArgs args) {
   using C = TgmmTile<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&map_x);
     tma_prefetch_desc(&map_dy);
+    tma_prefetch_desc(&map_dw);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -190,50 +193,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = pw >> 2;
     const int quad = warp & 3;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-    uint8_t* srow = staging + (h * kBM + quad * 32 + lane) * C::kStageRow;
+    uint8_t* box = staging + pw * 4096;
+    uint8_t* brow = box + lane * 128;  // this thread's row of the box
     uint32_t t = 0;
     for (long long u = blockIdx.x; u < num_units; u += gridDim.x) {
       const int g = static_cast<int>(u / (KT * NT));
       const int rem = static_cast<int>(u % (KT * NT));
       const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
       const int r0 = offsets[g], r1 = offsets[g + 1];
-      const long long krow = static_cast<long long>(g) * args.K + k0 + quad * 32 + lane;
-      uint16_t* dst = args.dw + krow * args.N + n0 + h * (BN / 2);
-      if (r1 <= r0) {
-        bulk_wait_read_all();
-#pragma unroll
-        for (int j = 0; j < BN / 16; ++j) reinterpret_cast<uint4*>(srow)[j] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-        bulk_copy_s2g(dst, srow, BN);
-        bulk_commit();
-        continue;
-      }
-      const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, abort_word, lim))) break;
-      tc_fence_after();
+      const int y = g * args.K + k0 + quad * 32;
       uint32_t r[BN / 2];
+      if (r1 <= r0) {
 #pragma unroll
-      for (int cc = 0; cc < BN / 64; ++cc)
-        tmem_ld_32x32(t_lane + b * BN + h * (BN / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * cc));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
-      ++t;
-      bulk_wait_read_all();
+        for (int j = 0; j < BN / 2; ++j) r[j] = 0u;
+      } else {
+        const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, abort_word, lim))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int j = 0; j < BN / 2; j += 8) {
-        reinterpret_cast<uint4*>(srow)[j / 8] =
-            make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                       pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                       pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
-                       pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+        for (int cc = 0; cc < BN / 64; ++cc)
+          tmem_ld_32x32(t_lane + b * BN + h * (BN / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * cc));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        ++t;
       }
-      fence_proxy_async_smem();
-      bulk_copy_s2g(dst, srow, BN);
-      bulk_commit();
+      // one 64-column box per pass; 16-byte chunk j of a row sits at chunk
+      // position j ^ (row & 7) (the 128-byte swizzle of the dW tensor map)
+#pragma unroll
+      for (int pass = 0; pass < BN / 128; ++pass) {
+        if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = 64 * pass + 8 * j;
+          *reinterpret_cast<uint4*>(brow + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])),
+                         pack_bf16x2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])),
+                         pack_bf16x2(__uint_as_float(r[c + 4]), __uint_as_float(r[c + 5])),
+                         pack_bf16x2(__uint_as_float(r[c + 6]), __uint_as_float(r[c + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_dw, box, n0 + h * (BN / 2) + 64 * pass, y);
+          bulk_commit();
+        }
+      }
     }
-    bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -246,12 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN>
-cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args, int grid,
+cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
+                   const TgmmArgs& args, int grid,
                    cudaStream_t stream) {
   constexpr int smem = TgmmTile<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(tgmm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tgmm_kernel<BN><<<grid, kThreads, smem, stream>>>(map_x, map_dy, args);
+  tgmm_kernel<BN><<<grid, kThreads, smem, stream>>>(map_x, map_dy, map_dw, args);
   return cudaGetLastError();
 }
 
@@ -259,10 +269,11 @@ cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const Tg
 
 int tgmm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
 
-cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const TgmmArgs& args, int grid,
+cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
+                             const TgmmArgs& args, int grid,
                              cudaStream_t stream) {
-  if (args.N % 256 == 0) return launch<256>(map_x, map_dy, args, grid, stream);
-  return launch<128>(map_x, map_dy, args, grid, stream);
+  if (args.N % 256 == 0) return launch<256>(map_x, map_dy, map_dw, args, grid, stream);
+  return launch<128>(map_x, map_dy, map_dw, args, grid, stream);
 }
 
 }  // namespace gmm

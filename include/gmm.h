@@ -213,6 +213,19 @@ gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const void* wq, 
                                int fuse_silu_mul, void* out, void* stream);
 
 /*
+ * Diagnostic of the failure path (the pages have no counterpart: this checks
+ * the library's own safety mechanism).  Launches one small kernel whose
+ * threads wait, through the same bounded wait every kernel of this library
+ * uses, on a barrier that nothing ever completes: after limit_ms (1..10000)
+ * the wait gives up, the other waiting warps stop through the shared abort
+ * word, GMM_ERR_TIMEOUT's bit is set in the workspace's sticky error word and
+ * the kernel returns; gmm_get_device_status() then reports GMM_ERR_TIMEOUT.
+ * The GPU context stays usable.  workspace: any zero-initialised workspace
+ * (at least 16 bytes).
+ */
+gmm_status gmm_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int limit_ms, void* stream);
+
+/*
  * Synchronizes `stream`, reads the workspace's sticky error word, clears it
  * and maps it to a status: GMM_ERR_TIMEOUT if a wait ran out, else
  * GMM_ERR_GROUP_SIZES if some call saw invalid group sizes, else GMM_OK.
