@@ -66,7 +66,10 @@ struct Fp8Tile {
   static constexpr int kStages = BN == 256 ? 3 : 4;
   static constexpr int kRowBytes = FUSE ? BN / 4 * 2 : BN;  // bf16 bytes per thread row
   static constexpr int kStageRow = kRowBytes + 16;         // padded: conflict-free 16-byte stores
-  static constexpr int kStagingBytes = 8 * 32 * kStageRow;
+  // plain epilogue: per warp BN/128 boxes of 32 rows x 64 bf16 (4 KB each,
+  // 128-byte swizzle) written by TMA tensor stores
+  static constexpr int kBoxes = BN / 128;
+  static constexpr int kStagingBytes = FUSE ? 8 * 32 * kStageRow : 8 * kBoxes * 4096;
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -85,7 +88,7 @@ struct Fp8Tile {
 template <int BN, bool FUSE, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gmm_fp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const FwdArgs args) {
+                   const __grid_constant__ CUtensorMap map_out, const FwdArgs args) {
   static_assert(!QUANT || (FUSE && BN == 256), "the quantized output is for the fused 128-column units");
   using C = Fp8Tile<BN, FUSE, QUANT>;
   constexpr int SEG = C::kSeg;
@@ -403,22 +406,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h == 0) args.hs[static_cast<long long>(n0 / 128) * args.M + row] = sc;
           }
         }
+        __syncwarp();
+        const int wrow0 = tl.row0 + quad * 32;
+        const int nvalid = args.out ? max(0, min(32, tl.row1 - wrow0)) : 0;
+        uint16_t* gdst = args.out + static_cast<long long>(wrow0) * args.N + n0 + h * SEG;
+        warp_store_rows<C::kRowBytes, C::kStageRow>(wstage, reinterpret_cast<uint8_t*>(gdst),
+                                                    static_cast<long long>(args.N) * 2, nvalid, lane);
+        __syncwarp();
       } else {
+        // the warp's 32 rows x BN/2 columns -> kBoxes swizzled 32x64 boxes;
+        // 16-byte chunk j of row r sits at chunk position j ^ (r & 7)
+        uint8_t* wbox = staging + pw * C::kBoxes * 4096;
+        if (lane == 0) bulk_wait_read_all();  // the previous unit's stores have read the boxes
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < SEG; j += 4) {
-          reinterpret_cast<uint4*>(srow)[j / 4] =
-              make_uint4(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j + 1].x, acc[j + 1].y),
-                         pack_bf16x2(acc[j + 2].x, acc[j + 2].y), pack_bf16x2(acc[j + 3].x, acc[j + 3].y));
+        for (int i = 0; i < C::kBoxes; ++i) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int p2 = 32 * i + 4 * j;  // float2 index of column 64 i + 8 j
+            *reinterpret_cast<uint4*>(wbox + i * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(acc[p2].x, acc[p2].y), pack_bf16x2(acc[p2 + 1].x, acc[p2 + 1].y),
+                           pack_bf16x2(acc[p2 + 2].x, acc[p2 + 2].y), pack_bf16x2(acc[p2 + 3].x, acc[p2 + 3].y));
+          }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int wrow0 = tl.row0 + quad * 32;
+        const int nvalid = max(0, min(32, tl.row1 - wrow0));
+        const int col0 = n0 + h * (BN / 2);
+        // Full 32-row boxes go out as TMA tensor stores, ragged ones (the next
+        // group follows) as masked 16-byte stores.  The two are independent
+        // tests on a flag taken from lane 0 rather than an if/else: the
+        // if/else form was measured to run both arms in every warp.
+        const bool full = __shfl_sync(0xffffffffu, nvalid, 0) == 32;
+        if (full && lane == 0) {
+#pragma unroll
+          for (int i = 0; i < C::kBoxes; ++i) tma_store_2d(&map_out, wbox + i * 4096, col0 + 64 * i, wrow0);
+          bulk_commit();
+        }
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < C::kBoxes; ++i) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int r = it * 4 + (lane >> 3), j = lane & 7;
+              if (r < nvalid)
+                *reinterpret_cast<uint4*>(args.out + static_cast<long long>(wrow0 + r) * args.N + col0 + 64 * i +
+                                          8 * j) =
+                    *reinterpret_cast<const uint4*>(wbox + i * 4096 + r * 128 + ((j ^ (r & 7)) << 4));
+            }
+          }
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      const int wrow0 = tl.row0 + quad * 32;
-      const int nvalid = args.out ? max(0, min(32, tl.row1 - wrow0)) : 0;
-      uint16_t* gdst = args.out + static_cast<long long>(wrow0) * args.N + n0 + (FUSE ? h * SEG : h * (BN / 2));
-      warp_store_rows<C::kRowBytes, C::kStageRow>(wstage, reinterpret_cast<uint8_t*>(gdst),
-                                                  static_cast<long long>(args.N) * 2, nvalid, lane);
-      __syncwarp();
     }
+    if (!FUSE && lane == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown
@@ -432,13 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, bool FUSE, bool QUANT>
-cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
-                   cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                   const FwdArgs& args, int grid, cudaStream_t stream) {
   constexpr int smem = Fp8Tile<BN, FUSE, QUANT>::kSmemBytes;
   cudaError_t e =
       cudaFuncSetAttribute(gmm_fp8_kernel<BN, FUSE, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gmm_fp8_kernel<BN, FUSE, QUANT><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
+  gmm_fp8_kernel<BN, FUSE, QUANT><<<grid, kThreads, smem, stream>>>(map_a, map_b, map_out, args);
   return cudaGetLastError();
 }
 
@@ -450,12 +492,12 @@ Fp8Geometry fp8_geometry(int N, int fuse) {
   return {128, 128, 128};
 }
 
-cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
-                           cudaStream_t stream) {
-  if (args.fuse && args.hq) return launch<256, true, true>(map_a, map_b, args, grid, stream);
-  if (args.fuse) return launch<256, true, false>(map_a, map_b, args, grid, stream);
-  if (args.N % 256 == 0) return launch<256, false, false>(map_a, map_b, args, grid, stream);
-  return launch<128, false, false>(map_a, map_b, args, grid, stream);
+cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                           const FwdArgs& args, int grid, cudaStream_t stream) {
+  if (args.fuse && args.hq) return launch<256, true, true>(map_a, map_b, map_out, args, grid, stream);
+  if (args.fuse) return launch<256, true, false>(map_a, map_b, map_out, args, grid, stream);
+  if (args.N % 256 == 0) return launch<256, false, false>(map_a, map_b, map_out, args, grid, stream);
+  return launch<128, false, false>(map_a, map_b, map_out, args, grid, stream);
 }
 
 }  // namespace gmm

@@ -40,8 +40,10 @@ struct TgmmArgs {
 };
 
 // Host launchers: `grid` CTAs (persistent), on `stream`.  Return the launch error.
-cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
-                           cudaStream_t stream);
+// map_out: bf16 output [M, N], box 64 columns x 32 rows, 128-byte swizzle
+// (read by the plain epilogue only; the fused ones ignore it).
+cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                           const FwdArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                             cudaStream_t stream);
 // bf16 dgrad: the forward kernel with a K-major weight ([G*N_out, K] view);

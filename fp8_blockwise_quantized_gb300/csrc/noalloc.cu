@@ -82,12 +82,13 @@ gmm_status noalloc_setup(NoAllocDevice* out, EncodeTiledFn* encode) {
 }
 
 gmm_status encode(EncodeTiledFn fn, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint32_t box_inner, uint32_t box_outer) {
+                  uint32_t box_inner, uint32_t box_outer, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  uint64_t elem_bytes = 1) {
   cuuint64_t dims[2] = {inner, outer < 1 ? 1 : outer};
-  cuuint64_t strides[1] = {inner};
+  cuuint64_t strides[1] = {inner * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
@@ -127,9 +128,10 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse);
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_b, map_out;
   if ((st = encode(fn, &map_a, xq, K, M, 128, 128)) != GMM_OK) return st;
   if ((st = encode(fn, &map_b, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK) return st;
+  if ((st = encode(fn, &map_out, out, N, M, 64, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2)) != GMM_OK) return st;
   FwdArgs a{};
   a.xs = xs;
   a.ws = ws;
@@ -143,5 +145,5 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   a.wait_limit_ns = kDefaultWaitLimitNs;
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
   const int grid = static_cast<int>(max_units < d.sms ? max_units : d.sms);
-  return launch_gmm_fp8(map_a, map_b, a, grid, s) == cudaSuccess ? GMM_OK : GMM_ERR_CUDA;
+  return launch_gmm_fp8(map_a, map_b, map_out, a, grid, s) == cudaSuccess ? GMM_OK : GMM_ERR_CUDA;
 }
