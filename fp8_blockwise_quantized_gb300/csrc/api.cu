@@ -369,6 +369,8 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
                      int64_t N, void* dw, void* workspace, size_t workspace_bytes, void* stream) {
   gmm_status st = check_grouped(G, M, K, N, N);
   if (st != GMM_OK) return st;
+  // the kernel walks its output tiles with 32-bit indices
+  if (static_cast<int64_t>(G) * (K / 128) * (N / tgmm_bn(static_cast<int>(N))) > INT32_MAX / 2) return GMM_ERR_SHAPE;
   if (!dw || !group_sizes) return GMM_ERR_NULL;
   if (M > 0 && (!x || !dy)) return GMM_ERR_NULL;
   if (!aligned16(x) || !aligned16(dy) || !aligned16(dw) || !aligned16(group_sizes)) return GMM_ERR_ALIGN;

@@ -9,10 +9,11 @@
 // reduction walks the group's rows in chunks of 64:
 //   warp 0     TMA: x[rows, 128 k] as two 64x64 boxes and dy[rows, BN n] as
 //              BN/64 boxes; both land MN-major (K of the MMA = the row index).
-//   warp 1     on the group's last, partial chunk, zeroes the dy rows that
+//   warp 1     tcgen05.mma kind::f16, M=128 (k), N=BN (n), K=16 (rows).  On
+//              the group's last, partial chunk it skips the 16-row steps past
+//              the group's end and zeroes the x rows of the last step that
 //              belong to the next group (whole 128-byte rows, so the swizzle
-//              does not matter) and fences them into the async proxy; then
-//              tcgen05.mma kind::f16, M=128 (k), N=BN (n), K=16 (rows).
+//              does not matter), fenced into the async proxy.
 //   warps 2-9  epilogue: tcgen05.ld -> bf16 -> the warp's 32 rows staged in
 //              shared memory one 32x64 box at a time (128-byte swizzle) -> one
 //              TMA tensor store per box; zero tile for an empty group.  The
@@ -33,6 +34,42 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kChunk = 64;  // rows per stage
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+
+// This CTA's units u = blockIdx.x, + gridDim.x, ... (u / per_group is the
+// group).  The next unit's group offsets are loaded one unit ahead, so their
+// global-memory latency overlaps the current unit instead of sitting between
+// two units on each role's critical path.
+struct UnitWalk {
+  const int* offsets;
+  int per_group, num, u, g, r0, r1, gn, r0n, r1n;
+  __device__ UnitWalk(const int* off, int per_group_units, int num_units)
+      : offsets(off), per_group(per_group_units), num(num_units), u(blockIdx.x), g(0), r0(0), r1(0) {
+    if (u < num) {
+      g = u / per_group;
+      r0 = __ldg(offsets + g);
+      r1 = __ldg(offsets + g + 1);
+    }
+    prefetch();
+  }
+  __device__ bool live() const { return u < num; }
+  __device__ void prefetch() {
+    const int un = u + static_cast<int>(gridDim.x);
+    gn = 0;
+    r0n = r1n = 0;
+    if (un < num) {
+      gn = un / per_group;
+      r0n = __ldg(offsets + gn);
+      r1n = __ldg(offsets + gn + 1);
+    }
+  }
+  __device__ void next() {
+    u += static_cast<int>(gridDim.x);
+    g = gn;
+    r0 = r0n;
+    r1 = r1n;
+    prefetch();
+  }
+};
 
 template <int BN>
 struct TgmmTile {
@@ -93,8 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   const bool valid_meta = args.meta[kWsValid] != 0;
-  const int KT = args.K / 128, NT = args.N / BN;
-  const long long num_units = valid_meta ? static_cast<long long>(args.G) * KT * NT : 0;
+  const int KT = args.K / 128, NT = args.N / BN, KTNT = KT * NT;
+  // G * KT * NT < 2^31 (checked by the host)
+  const int num_units = valid_meta ? args.G * KTNT : 0;
   const int* offsets = args.meta + kWsOffsets;
   const uint64_t lim = args.wait_limit_ns;
 
@@ -102,11 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int g = static_cast<int>(u / (KT * NT));
-        const int rem = static_cast<int>(u % (KT * NT));
+      UnitWalk w(offsets, KTNT, num_units);
+      for (; w.live() && ok; w.next()) {
+        const int rem = w.u - w.g * KTNT;
         const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
-        const int r0 = offsets[g], r1 = offsets[g + 1];
+        const int r0 = w.r0, r1 = w.r1;
         for (int r = r0; r < r1; r += kChunk) {
           const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_word, lim)) {
@@ -136,9 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, kBM, BN);
     uint32_t c = 0, t = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const int g = static_cast<int>(u / (KT * NT));
-      const int r0 = offsets[g], r1 = offsets[g + 1];
+    UnitWalk w(offsets, KTNT, num_units);
+    for (; w.live() && ok; w.next()) {
+      const int r0 = w.r0, r1 = w.r1;
       if (r1 <= r0) continue;  // empty group: the epilogue writes zeros
       const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&tempty[b], tph ^ 1u, abort_word, lim))) break;
@@ -152,13 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* a_ptr = ring + s * C::kStageBytes;
         uint8_t* b_ptr = a_ptr + C::kABytes;
-        const int live = r1 - r;  // rows of this chunk that belong to group g
-        if (live < kChunk) {
-          // zero dy rows [live, 64) of every box: 128 bytes per row
-          const int nbytes16 = (kChunk - live) * 8;  // 16-byte words per box
-          for (int i = 0; i < BN / 64; ++i) {
-            uint4* p = reinterpret_cast<uint4*>(b_ptr + i * C::kBoxBytes + live * 128);
-            for (int w = lane; w < nbytes16; w += 32) p[w] = make_uint4(0, 0, 0, 0);
+        // rows of this chunk that belong to group g; the 16-row MMA steps past
+        // them are skipped and the rest of the last step's rows (the next
+        // group's) are zeroed in both x boxes (128 bytes per row and box)
+        const int live = r1 - r;
+        const int steps = live < kChunk ? (live + 15) / 16 : 4;
+        if (live < 16 * steps) {
+          const int words = (16 * steps - live) * 8;  // 16-byte words per box
+          for (int i = 0; i < 2; ++i) {
+            uint4* p = reinterpret_cast<uint4*>(a_ptr + i * C::kBoxBytes + live * 128);
+            for (int w = lane; w < words; w += 32) p[w] = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -169,8 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_u32(b_ptr);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            mma_bf16(d, smem_desc_sw128(a_addr + 2048 * j, C::kBoxBytes, 1024),
-                     smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024), idesc, (r > r0 || j > 0) ? 1u : 0u);
+            if (j < steps)
+              mma_bf16(d, smem_desc_sw128(a_addr + 2048 * j, C::kBoxBytes, 1024),
+                       smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024), idesc, (r > r0 || j > 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
         }
@@ -196,11 +238,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* box = staging + pw * 4096;
     uint8_t* brow = box + lane * 128;  // this thread's row of the box
     uint32_t t = 0;
-    for (long long u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const int g = static_cast<int>(u / (KT * NT));
-      const int rem = static_cast<int>(u % (KT * NT));
+    UnitWalk w(offsets, KTNT, num_units);
+    for (; w.live(); w.next()) {
+      const int g = w.g;
+      const int rem = w.u - g * KTNT;
       const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
-      const int r0 = offsets[g], r1 = offsets[g + 1];
+      const int r0 = w.r0, r1 = w.r1;
       const int y = g * args.K + k0 + quad * 32;
       uint32_t r[BN / 2];
       if (r1 <= r0) {

@@ -174,6 +174,8 @@ gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_si
  *   dw[g][k,n] = bf16( sum_{m in group g} x[m,k] * dy[m,n] ), fp32 accumulation;
  *   dw[g] = 0 for an empty group.
  *   x   bf16 [M, K];  dy  bf16 [M, N];  dw  bf16 [G, K, N]
+ * GMM_ERR_SHAPE also when G * (K/128) * (N/256, or N/128 when N % 256 != 0)
+ * output tiles exceed 2^30.
  */
 gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M,
                      int64_t K, int64_t N, void* dw, void* workspace, size_t workspace_bytes,
