@@ -335,6 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32(tb + (ca < CPS ? tcol0 + 32 * ca : tcol1 + 32 * (ca - CPS)), ra);
           tmem_ld_32x32(tb + (cb < CPS ? tcol0 + 32 * cb : tcol1 + 32 * (cb - CPS)), rb);
           tmem_ld_wait();
+          if (pc == NCH - 2) {
+            // the K block's partial is in registers: hand the buffer and the
+            // scale slot back before the last multiply-adds
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&tempty[b]);
+              mbar_arrive(&sempty[sl]);
+            }
+          }
           const float2 fa = ca < CPS ? make_float2(f0, f0) : make_float2(f1, f1);
           const float2 fb = cb < CPS ? make_float2(f0, f0) : make_float2(f1, f1);
 #pragma unroll
@@ -347,12 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[16 * cb + i] =
                 __ffma2_rn(make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])), fb,
                            acc[16 * cb + i]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tempty[b]);
-          mbar_arrive(&sempty[sl]);
         }
         ++t;
       }
