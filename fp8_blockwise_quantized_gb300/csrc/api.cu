@@ -268,10 +268,17 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), 1);
-  CUtensorMap map_a, map_b;
+  CUtensorMap map_a, map_b, map_h;
   if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
   if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
     return st;
+  // h (when requested) is written through its own tensor map; without h the
+  // kernel stores only hq and hs and never reads map_h
+  if (h) {
+    if ((st = encode_2d(&map_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, N, M, 64, 32)) != GMM_OK) return st;
+  } else {
+    map_h = map_a;
+  }
   FwdArgs a{};
   a.xs = xs;
   a.ws = ws;
@@ -287,8 +294,7 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   a.wait_limit_ns = wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
   const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
-  // the fused epilogue does not use an output tensor map
-  cudaError_t e = launch_gmm_fp8(map_a, map_b, map_a, a, grid, s);
+  cudaError_t e = launch_gmm_fp8(map_a, map_b, map_h, a, grid, s);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 fused-quant kernel launch");
 }
 

@@ -61,6 +61,29 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 
+// max |v| over the 8 bf16 values of a 16-byte chunk
+__device__ __forceinline__ float bf16x8_absmax(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+  return m;
+}
+// 8 bf16 values (a 16-byte chunk) -> 8 e4m3 codes: e4m3(fp32(v) * inv)
+__device__ __forceinline__ uint2 bf16x8_to_e4m3(uint4 v, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t q[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t p0 = w[2 * i], p1 = w[2 * i + 1];
+    q[i] = e4m3x2(__fmul_rn(__uint_as_float(p0 << 16), inv), __fmul_rn(__uint_as_float(p0 & 0xffff0000u), inv)) |
+           (e4m3x2(__fmul_rn(__uint_as_float(p1 << 16), inv), __fmul_rn(__uint_as_float(p1 & 0xffff0000u), inv))
+            << 16);
+  }
+  return make_uint2(q[0], q[1]);
+}
+
 // silu(v) = v / (1 + exp(-v)), with the fast hardware exponential and divide
 // (relative error a few ulp of fp32, far below the bf16 rounding that
 // follows).  Saturates correctly: exp(-v) = inf gives 0.

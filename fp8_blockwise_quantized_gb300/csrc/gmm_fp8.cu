@@ -21,13 +21,17 @@
 //               row scales xs[kb, rows] and its RHS block scales into a
 //               shared-memory ring that runs ahead of the MMAs (the scales are
 //               then never a global-memory load on the promotion's path).
-//   warp 3      idle (completes warpgroup 0, which hands most of its
-//               registers to the promotion warpgroups).
+//   warp 3      store warp: takes each unit's staged bf16 output boxes to
+//               global memory (TMA tensor stores for full 32-row boxes, masked
+//               stores for ragged ones: the tile may run into the next group)
+//               and, for the quantized output, re-reads the staged bf16 rows
+//               to cast them to e4m3 with 1x128 absmax scales.
 //   warps 4-11  promotion: tcgen05.ld the partial (one TMEM lane = one row),
 //               FMA it into fp32 registers with the scale product, release the
-//               buffer; after the last K block convert and store the rows
-//               row0..row1 of the tile (masked: the tile may run into the next
-//               group), and zero the output rows that no group covers.
+//               buffer; after the last K block convert the accumulators to
+//               bf16 (silu(gate) * up when fused) into swizzled 32x64 staging
+//               boxes and go on with the next unit while the store warp
+//               drains them.  They also zero the output rows no group covers.
 // Work units (tile, column block) are dealt round-robin to a persistent grid
 // of one CTA per SM, tile-major so that the units sharing an Xq tile and the
 // tiles sharing an expert's Wq columns run at the same time (L2 reuse).
@@ -45,31 +49,59 @@ constexpr int kThreads = 384;
 constexpr int kPromoWarps = 8;
 constexpr int kPromoWarp0 = 4;   // first promotion warp
 // Register split: the launch gives 168 registers per thread (three warps per
-// SM sub-partition); warpgroup 0 (TMA, MMA, two idle warps) gives most of its
+// SM sub-partition); warpgroup 0 (TMA, MMA, scales, stores) gives most of its
 // share to the two promotion warpgroups, which hold the fp32 accumulators:
 // 128 x control + 256 x promo <= 384 x 168 = 64512.
 template <int BN>
 struct RegSplit {
-  static constexpr uint32_t kControl = BN == 256 ? 40 : 72;
-  static constexpr uint32_t kPromo = BN == 256 ? 232 : 216;
+  static constexpr uint32_t kControl = BN == 256 ? 56 : 72;
+  static constexpr uint32_t kPromo = BN == 256 ? 224 : 216;
   static_assert(128 * kControl + 256 * kPromo <= 384 * 168, "register split exceeds the launch budget");
 };
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kScaleSlots = 8;        // K blocks of scales in flight
 constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
 
+// This CTA's units u = blockIdx.x, + gridDim.x, ... (tile u / per_tile,
+// column block u % per_tile).  The next unit's tile is loaded one unit ahead,
+// so its global-memory latency overlaps the current unit instead of sitting
+// between two units on each role's path.
+struct TileWalk {
+  const Tile* tiles;
+  long long num, u;
+  int per;
+  Tile cur, nxt;
+  __device__ TileWalk(const Tile* t, int per_tile, long long num_units)
+      : tiles(t), num(num_units), u(blockIdx.x), per(per_tile) {
+    if (u < num) cur = load(u);
+    prefetch();
+  }
+  __device__ Tile load(long long v) const {
+    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + v / per));
+    return Tile{q.x, q.y, q.z, q.w};
+  }
+  __device__ void prefetch() {
+    const long long un = u + gridDim.x;
+    if (un < num) nxt = load(un);
+  }
+  __device__ bool live() const { return u < num; }
+  __device__ int col0(int cols) const { return static_cast<int>(u % per) * cols; }
+  __device__ void next() {
+    u += gridDim.x;
+    cur = nxt;
+    prefetch();
+  }
+};
+
 template <int BN, bool FUSE, bool QUANT>
 struct Fp8Tile {
-  // The epilogue stages each warp's 32 output rows in shared memory and
-  // writes them with warp-cooperative 512-byte stores.  Its staging takes the
-  // room of one ring slot when BN = 256 (the MMA rarely waits for the ring).
+  // The epilogue stages each promotion warp's 32 output rows as bf16 boxes of
+  // 32 rows x 64 columns (4 KB, 128-byte swizzle): BN/128 boxes per warp, or
+  // one box of h when fused.  The staging takes the room of one ring slot
+  // when BN = 256 (the MMA rarely waits for the ring).
   static constexpr int kStages = BN == 256 ? 3 : 4;
-  static constexpr int kRowBytes = FUSE ? BN / 4 * 2 : BN;  // bf16 bytes per thread row
-  static constexpr int kStageRow = kRowBytes + 16;         // padded: conflict-free 16-byte stores
-  // plain epilogue: per warp BN/128 boxes of 32 rows x 64 bf16 (4 KB each,
-  // 128-byte swizzle) written by TMA tensor stores
-  static constexpr int kBoxes = BN / 128;
-  static constexpr int kStagingBytes = FUSE ? 8 * 32 * kStageRow : 8 * kBoxes * 4096;
+  static constexpr int kBoxes = FUSE ? 1 : BN / 128;
+  static constexpr int kStagingBytes = 8 * kBoxes * 4096;
   static constexpr int kABytes = kBM * 128;
   static constexpr int kBBytes = BN * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -78,11 +110,7 @@ struct Fp8Tile {
   static constexpr int kTmemCols = 2 * BN;             // two partial buffers
   static constexpr int kBarBytes = 512;
   static constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
-  // fused quantized output: the two column halves of a row's 1x128 block meet
-  // through a double-buffered absmax exchange
-  static constexpr int kExchangeBytes = QUANT ? 2 * 2 * kBM * 4 : 0;
-  static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kExchangeBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kBarBytes;
 };
 
 template <int BN, bool FUSE, bool QUANT>
@@ -98,15 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem;
   uint8_t* staging = smem + kStages * C::kStageBytes;
   float* scales = reinterpret_cast<float*>(staging + C::kStagingBytes);
-  float* amax_x = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scales) + C::kScaleBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(amax_x) + C::kExchangeBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scales) + C::kScaleBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kScaleSlots;
-  uint64_t* ebar = sempty + kScaleSlots;  // absmax exchange of the fused quantized output
-  uint64_t* drain = ebar + 1;
+  uint64_t* staged = sempty + kScaleSlots;  // a unit's output boxes are in the staging area
+  uint64_t* sfree = staged + 1;             // the store warp has emptied the staging area
+  uint64_t* drain = sfree + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -124,12 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sfull[q], 32);  // one cp.async arrival per loader lane
       mbar_init(&sempty[q], kPromoWarps);
     }
-    mbar_init(ebar, kPromoWarps);
+    mbar_init(staged, kPromoWarps);
+    mbar_init(sfree, 1);
     mbar_init(drain, 1);
     *abort_word = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_out);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -153,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const Tile tl = args.tiles[u / units_per_tile];
-        const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+      for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+        const Tile tl = w.cur;
+        const int n0 = w.col0(C::kOutCols);
         const int brow = tl.g * Nw + n0;
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
@@ -229,9 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NBw = Nw / 128;
     uint32_t q = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Tile tl = args.tiles[u / units_per_tile];
-      const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+      const Tile tl = w.cur;
+      const int n0 = w.col0(C::kOutCols);
       // the (up to) two RHS column blocks this unit's accumulators use
       const int wb0 = n0 / 128;
       const int wb1 = FUSE ? (args.N + n0) / 128 : (BN == 256 ? n0 / 128 + 1 : n0 / 128);
@@ -258,6 +288,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     cp_async_wait_all();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ store warp
+    uint32_t ue = 0;
+    bool ok = true;
+    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+      const Tile tl = w.cur;
+      const int n0 = w.col0(C::kOutCols);
+      if (!__all_sync(0xffffffffu, mbar_wait(staged, ue & 1u, abort_word, lim))) {
+        ok = false;
+        break;
+      }
+      if (args.out) {
+        // box region of promotion warp p: rows (p & 3) * 32.., columns
+        // n0 + (p >> 2) * 64 * kBoxes..; chunk j of row r at j ^ (r & 7).
+        // Full 32-row boxes: one TMA tensor store per box, issued by lanes
+        // in parallel (lane = p * kBoxes + box).
+        if (lane < kPromoWarps * C::kBoxes) {
+          const int p = lane / C::kBoxes, i = lane % C::kBoxes;
+          const int wrow0 = tl.row0 + (p & 3) * 32;
+          if (tl.row1 - wrow0 >= 32) {
+            tma_store_2d(&map_out, staging + (p * C::kBoxes + i) * 4096, n0 + (p >> 2) * 64 * C::kBoxes + 64 * i,
+                         wrow0);
+            bulk_commit();
+          }
+        }
+        // ragged boxes (the tile runs into the next group): masked stores
+#pragma unroll 1
+        for (int p = 0; p < kPromoWarps; ++p) {
+          const int wrow0 = tl.row0 + (p & 3) * 32;
+          const int nvalid = min(32, tl.row1 - wrow0);
+          if (nvalid > 0 && nvalid < 32) {
+            const uint8_t* wbox = staging + p * C::kBoxes * 4096;
+            const int col0 = n0 + (p >> 2) * 64 * C::kBoxes;
+#pragma unroll 1
+            for (int i = 0; i < C::kBoxes; ++i) {
+#pragma unroll 1
+              for (int it = 0; it < 8; ++it) {
+                const int r = it * 4 + (lane >> 3), j = lane & 7;
+                if (r < nvalid)
+                  *reinterpret_cast<uint4*>(args.out + static_cast<long long>(wrow0 + r) * args.N + col0 + 64 * i +
+                                            8 * j) =
+                      *reinterpret_cast<const uint4*>(wbox + i * 4096 + r * 128 + ((j ^ (r & 7)) << 4));
+              }
+            }
+          }
+        }
+      }
+      if (QUANT) {
+        // h's 1x128 block of row r is the unit's 128 columns: box (r >> 5)
+        // holds columns 0-63, box 4 + (r >> 5) columns 64-127.  Quantized
+        // exactly as gmm_quantize_lhs would: absmax of the bf16 values / 448.
+        const int nrows = tl.row1 - tl.row0;
+        for (int r = lane; r < nrows; r += 32) {
+          const int rr = r & 31, sw = r & 7;
+          const uint8_t* b0 = staging + (r >> 5) * 4096 + rr * 128;
+          const uint8_t* b1 = b0 + 4 * 4096;
+          float amax = 0.0f;
+#pragma unroll 2
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v0 = *reinterpret_cast<const uint4*>(b0 + ((j ^ sw) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(b1 + ((j ^ sw) << 4));
+            amax = fmaxf(amax, fmaxf(bf16x8_absmax(v0), bf16x8_absmax(v1)));
+          }
+          float sc, inv;
+          e4m3_block_scale(amax, sc, inv);
+          uint8_t* qrow = args.hq + static_cast<long long>(tl.row0 + r) * args.N + n0;
+#pragma unroll 2
+          for (int j = 0; j < 8; j += 2) {
+            const uint2 q0 = bf16x8_to_e4m3(*reinterpret_cast<const uint4*>(b0 + ((j ^ sw) << 4)), inv);
+            const uint2 q1 = bf16x8_to_e4m3(*reinterpret_cast<const uint4*>(b0 + (((j + 1) ^ sw) << 4)), inv);
+            const uint2 q2 = bf16x8_to_e4m3(*reinterpret_cast<const uint4*>(b1 + ((j ^ sw) << 4)), inv);
+            const uint2 q3 = bf16x8_to_e4m3(*reinterpret_cast<const uint4*>(b1 + (((j + 1) ^ sw) << 4)), inv);
+            *reinterpret_cast<uint4*>(qrow + 8 * j) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+            *reinterpret_cast<uint4*>(qrow + 64 + 8 * j) = make_uint4(q2.x, q2.y, q3.x, q3.y);
+          }
+          args.hs[static_cast<long long>(n0 / 128) * args.M + tl.row0 + r] = sc;
+        }
+      }
+      // the staging area may be overwritten once the tensor stores have read
+      // it (each issuing lane waits for its own) and every lane's reads are done
+      bulk_wait_read_all();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree);
+      ++ue;
+    }
+    bulk_wait_all();
   } else if (warp >= kPromoWarp0) {
     // ------------------------------------------------------------ promotion + epilogue
     regs_inc<RegSplit<BN>::kPromo>();
@@ -289,9 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t t = 0, ue = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const Tile tl = args.tiles[u / units_per_tile];
-      const int n0 = static_cast<int>(u % units_per_tile) * C::kOutCols;
+    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+      const Tile tl = w.cur;
       const int row = tl.row0 + quad * 32 + lane;
       const bool valid = row < tl.row1;
       int tcol0, tcol1, wsel0, wsel1;
@@ -361,110 +476,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++t;
       }
       if (!ok) break;
-      // epilogue: this thread's row -> staging, then the warp stores its rows
-      uint8_t* wstage = staging + pw * 32 * C::kStageRow;
-      uint8_t* srow = wstage + lane * C::kStageRow;
+      // epilogue: once the store warp has emptied the staging area, this
+      // warp's 32 rows go in as bf16 boxes (chunk j of row r at j ^ (r & 7))
+      if (!__all_sync(0xffffffffu, mbar_wait(sfree, (ue & 1u) ^ 1u, abort_word, lim))) break;
+      uint8_t* wbox = staging + pw * C::kBoxes * 4096 + lane * 128;
       if (FUSE) {
-        // gate = accumulators [0, SEG), up = [SEG, 2 SEG); h = bf16(silu(gate) * up)
-        uint32_t hb[SEG / 2];
-        float amax = 0.0f;
+        // gate = acc[0, SEG/2), up = acc[SEG/2, SEG) (pairs of columns);
+        // h = bf16(silu(gate) * up), SEG = 64 columns = one box row
 #pragma unroll
-        for (int j = 0; j < SEG; j += 2) {
-          const float2 gt = acc[j / 2], up = acc[(SEG + j) / 2];
-          hb[j / 2] = pack_bf16x2(silu_f32(gt.x) * up.x, silu_f32(gt.y) * up.y);
-          if (QUANT)
-            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb[j / 2] << 16)),
-                                     fabsf(__uint_as_float(hb[j / 2] & 0xffff0000u))));
-        }
+        for (int j = 0; j < 8; ++j) {
+          uint32_t hb[4];
 #pragma unroll
-        for (int j = 0; j < SEG / 8; ++j)
-          reinterpret_cast<uint4*>(srow)[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
-        if (QUANT) {
-          // the 1x128 block of this row spans both column halves (two warpgroups):
-          // exchange the halves' absmax, then quantize the bf16 values exactly as
-          // gmm_quantize_lhs would
-          float* ex = amax_x + (ue & 1u) * (2 * kBM);
-          ex[h * kBM + rit] = amax;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ebar);
-          if (!__all_sync(0xffffffffu, mbar_wait(ebar, ue & 1u, abort_word, lim))) break;
-          ++ue;
-          float sc, inv;
-          e4m3_block_scale(fmaxf(ex[rit], ex[kBM + rit]), sc, inv);
-          if (valid) {
-            uint4* qdst = reinterpret_cast<uint4*>(args.hq + static_cast<long long>(row) * args.N + n0 + h * SEG);
-#pragma unroll
-            for (int j = 0; j < SEG / 16; ++j) {
-              uint32_t w[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t p0 = hb[8 * j + 2 * i], p1 = hb[8 * j + 2 * i + 1];
-                w[i] = e4m3x2(__fmul_rn(__uint_as_float(p0 << 16), inv),
-                              __fmul_rn(__uint_as_float(p0 & 0xffff0000u), inv)) |
-                       (e4m3x2(__fmul_rn(__uint_as_float(p1 << 16), inv),
-                               __fmul_rn(__uint_as_float(p1 & 0xffff0000u), inv))
-                        << 16);
-              }
-              qdst[j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            if (h == 0) args.hs[static_cast<long long>(n0 / 128) * args.M + row] = sc;
+          for (int k = 0; k < 4; ++k) {
+            const float2 gt = acc[4 * j + k], up = acc[SEG / 2 + 4 * j + k];
+            hb[k] = pack_bf16x2(silu_f32(gt.x) * up.x, silu_f32(gt.y) * up.y);
           }
+          *reinterpret_cast<uint4*>(wbox + ((j ^ (lane & 7)) << 4)) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
         }
-        __syncwarp();
-        const int wrow0 = tl.row0 + quad * 32;
-        const int nvalid = args.out ? max(0, min(32, tl.row1 - wrow0)) : 0;
-        uint16_t* gdst = args.out + static_cast<long long>(wrow0) * args.N + n0 + h * SEG;
-        warp_store_rows<C::kRowBytes, C::kStageRow>(wstage, reinterpret_cast<uint8_t*>(gdst),
-                                                    static_cast<long long>(args.N) * 2, nvalid, lane);
-        __syncwarp();
       } else {
-        // the warp's 32 rows x BN/2 columns -> kBoxes swizzled 32x64 boxes;
-        // 16-byte chunk j of row r sits at chunk position j ^ (r & 7)
-        uint8_t* wbox = staging + pw * C::kBoxes * 4096;
-        if (lane == 0) bulk_wait_read_all();  // the previous unit's stores have read the boxes
-        __syncwarp();
 #pragma unroll
         for (int i = 0; i < C::kBoxes; ++i) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int p2 = 32 * i + 4 * j;  // float2 index of column 64 i + 8 j
-            *reinterpret_cast<uint4*>(wbox + i * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(wbox + i * 4096 + ((j ^ (lane & 7)) << 4)) =
                 make_uint4(pack_bf16x2(acc[p2].x, acc[p2].y), pack_bf16x2(acc[p2 + 1].x, acc[p2 + 1].y),
                            pack_bf16x2(acc[p2 + 2].x, acc[p2 + 2].y), pack_bf16x2(acc[p2 + 3].x, acc[p2 + 3].y));
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        const int wrow0 = tl.row0 + quad * 32;
-        const int nvalid = max(0, min(32, tl.row1 - wrow0));
-        const int col0 = n0 + h * (BN / 2);
-        // Full 32-row boxes go out as TMA tensor stores, ragged ones (the next
-        // group follows) as masked 16-byte stores.  The two are independent
-        // tests on a flag taken from lane 0 rather than an if/else: the
-        // if/else form was measured to run both arms in every warp.
-        const bool full = __shfl_sync(0xffffffffu, nvalid, 0) == 32;
-        if (full && lane == 0) {
-#pragma unroll
-          for (int i = 0; i < C::kBoxes; ++i) tma_store_2d(&map_out, wbox + i * 4096, col0 + 64 * i, wrow0);
-          bulk_commit();
-        }
-        if (!full) {
-#pragma unroll
-          for (int i = 0; i < C::kBoxes; ++i) {
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int r = it * 4 + (lane >> 3), j = lane & 7;
-              if (r < nvalid)
-                *reinterpret_cast<uint4*>(args.out + static_cast<long long>(wrow0 + r) * args.N + col0 + 64 * i +
-                                          8 * j) =
-                    *reinterpret_cast<const uint4*>(wbox + i * 4096 + r * 128 + ((j ^ (r & 7)) << 4));
-            }
-          }
-        }
-        __syncwarp();
       }
+      fence_proxy_async_smem();  // the tensor stores read the boxes through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(staged);
+      ++ue;
     }
-    if (!FUSE && lane == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ teardown

@@ -40,8 +40,8 @@ struct TgmmArgs {
 };
 
 // Host launchers: `grid` CTAs (persistent), on `stream`.  Return the launch error.
-// map_out: bf16 output [M, N], box 64 columns x 32 rows, 128-byte swizzle
-// (read by the plain epilogue only; the fused ones ignore it).
+// map_out: the bf16 output (out, or h when fused) [M, N], box 64 columns x
+// 32 rows, 128-byte swizzle; read only when args.out is not null.
 cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                            const FwdArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
