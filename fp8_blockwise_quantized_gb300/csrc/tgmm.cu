@@ -35,15 +35,15 @@ constexpr int kEpiWarps = 8;
 constexpr int kChunk = 64;  // rows per stage
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-// This CTA's units u = blockIdx.x, + gridDim.x, ... (u / per_group is the
+// This CTA's units u = first, first + stride, ... (u / per_group is the
 // group).  The next unit's group offsets are loaded one unit ahead, so their
 // global-memory latency overlaps the current unit instead of sitting between
 // two units on each role's critical path.
 struct UnitWalk {
   const int* offsets;
-  int per_group, num, u, g, r0, r1, gn, r0n, r1n;
-  __device__ UnitWalk(const int* off, int per_group_units, int num_units)
-      : offsets(off), per_group(per_group_units), num(num_units), u(blockIdx.x), g(0), r0(0), r1(0) {
+  int per_group, num, step, u, g, r0, r1, gn, r0n, r1n;
+  __device__ UnitWalk(const int* off, int per_group_units, int num_units, int first, int stride)
+      : offsets(off), per_group(per_group_units), num(num_units), step(stride), u(first), g(0), r0(0), r1(0) {
     if (u < num) {
       g = u / per_group;
       r0 = __ldg(offsets + g);
@@ -53,7 +53,7 @@ struct UnitWalk {
   }
   __device__ bool live() const { return u < num; }
   __device__ void prefetch() {
-    const int un = u + static_cast<int>(gridDim.x);
+    const int un = u + step;
     gn = 0;
     r0n = r1n = 0;
     if (un < num) {
@@ -63,7 +63,7 @@ struct UnitWalk {
     }
   }
   __device__ void next() {
-    u += static_cast<int>(gridDim.x);
+    u += step;
     g = gn;
     r0 = r0n;
     r1 = r1n;
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      UnitWalk w(offsets, KTNT, num_units);
+      UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
       for (; w.live() && ok; w.next()) {
         const int rem = w.u - w.g * KTNT;
         const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, kBM, BN);
     uint32_t c = 0, t = 0;
     bool ok = true;
-    UnitWalk w(offsets, KTNT, num_units);
+    UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
     for (; w.live() && ok; w.next()) {
       const int r0 = w.r0, r1 = w.r1;
       if (r1 <= r0) continue;  // empty group: the epilogue writes zeros
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* box = staging + pw * 4096;
     uint8_t* brow = box + lane * 128;  // this thread's row of the box
     uint32_t t = 0;
-    UnitWalk w(offsets, KTNT, num_units);
+    UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
     for (; w.live(); w.next()) {
       const int g = w.g;
       const int rem = w.u - g * KTNT;
@@ -297,6 +297,328 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (K a multiple of 256).  A cluster of two CTAs on the two
+// SMs of a pair owns the output tile (g, 256 rows of K, BN columns): each CTA
+// loads its own 128 k columns of x and half (BN/2) of the dy columns of every
+// 64-row chunk, and the even CTA issues one M=256 tcgen05.mma (cta_group::2)
+// per 16-row step over both CTAs' shared memory; each CTA's TMEM receives its
+// 128 k rows x BN.  A chunk takes 32 KB of each CTA's shared memory instead
+// of 48 KB, so the ring holds six chunks instead of four.
+//   warp 0     TMA producer (each CTA, its own halves into its own shared
+//              memory).  The even CTA's full[s] takes two arrivals: its own
+//              (with its bytes) and the odd CTA's, which for a whole chunk
+//              registers its bytes remotely and lets its copies complete on
+//              that barrier directly.
+//   warp 1     even CTA: wait full[s], zero the next group's x rows of a
+//              partial last step, issue the MMAs; commits arrive on both
+//              CTAs' empty[s] / tfull[b].  Odd CTA: a chunk whose last step
+//              holds rows of the next group lands on a local barrier; this
+//              warp zeroes those rows and then arrives on the even CTA's
+//              full[s].
+//   warps 2-9  epilogue (each CTA, its 128 k rows); the odd CTA's warps free
+//              the pair's TMEM buffer by remote arrives on the even CTA.
+constexpr int kPairStages = 6;
+
+// Zero rows [from, to) of both 64-row x boxes of a ring slot (128 bytes per
+// row and box, so the swizzle does not matter) and fence them into the async
+// proxy; the warp's lanes share the stores.
+__device__ __forceinline__ void zero_x_rows(uint8_t* a_ptr, int from, int to, int lane) {
+  constexpr int kBox = kChunk * 64 * 2;
+  const int words = (to - from) * 8;
+  for (int i = 0; i < 2; ++i) {
+    uint4* p = reinterpret_cast<uint4*>(a_ptr + i * kBox + from * 128);
+    for (int q = lane; q < words; q += 32) p[q] = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+}
+
+template <int BN>
+struct TgmmPairTile {
+  static constexpr int kBoxBytes = kChunk * 64 * 2;           // 64 rows x 64 bf16 = 8 KB
+  static constexpr int kABytes = 2 * kBoxBytes;               // this CTA's 128 k columns
+  static constexpr int kBBytes = (BN / 2 / 64) * kBoxBytes;   // this CTA's BN/2 n columns
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = BN == 256 ? kPairStages : 8;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kStagingBytes = kEpiWarps * 4096;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 512;
+};
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tgmm_pair_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dy,
+                     const __grid_constant__ CUtensorMap map_dw, const TgmmArgs args) {
+  using C = TgmmPairTile<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint8_t* staging = smem + S * C::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);  // even CTA: both halves ready
+  uint64_t* ploaded = full + S;  // odd CTA: a chunk to be zeroed landed
+  uint64_t* empty = ploaded + S;
+  uint64_t* tfull = empty + S;
+  uint64_t* tempty = tfull + 2;      // even CTA: both CTAs' epilogues freed buffer b
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 2);
+      mbar_init(&ploaded[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_word = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_x);
+    tma_prefetch_desc(&map_dy);
+    tma_prefetch_desc(&map_dw);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  const bool valid_meta = args.meta[kWsValid] != 0;
+  const int KP = args.K / 256, NT = args.N / BN, KPNT = KP * NT;
+  const int num_units = valid_meta ? args.G * KPNT : 0;
+  const int first = static_cast<int>(blockIdx.x >> 1), stride = static_cast<int>(gridDim.x >> 1);
+  const int* offsets = args.meta + kWsOffsets;
+  const uint64_t lim = args.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+      uint32_t c = 0;
+      bool ok = true;
+      UnitWalk w(offsets, KPNT, num_units, first, stride);
+      for (; w.live() && ok; w.next()) {
+        const int rem = w.u - w.g * KPNT;
+        const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128;
+        const int n0 = (rem % NT) * BN + static_cast<int>(rank) * (BN / 2);
+        for (int r = w.r0; r < w.r1; r += kChunk) {
+          const uint32_t s = c % S, ph = (c / S) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_word, lim)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = ring + s * C::kStageBytes;
+          uint8_t* b_dst = a_dst + C::kABytes;
+          const int live = w.r1 - r;
+          const bool zero = live < kChunk && (live & 15) != 0;  // last step holds next-group rows
+          if (leader || zero) {
+            // local completion: the even CTA's own half, or an odd-CTA chunk
+            // that warp 1 must zero before it counts
+            uint64_t* bar = leader ? &full[s] : &ploaded[s];
+            mbar_arrive_expect_tx(bar, C::kStageBytes);
+            tma_load_2d(a_dst, &map_x, bar, k0, r);
+            tma_load_2d(a_dst + C::kBoxBytes, &map_x, bar, k0 + 64, r);
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i) tma_load_2d(b_dst + i * C::kBoxBytes, &map_dy, bar, n0 + 64 * i, r);
+          } else {
+            // completes on the even CTA's barrier; the bytes may land before
+            // the expectation is registered (the count dips below zero
+            // within the phase)
+            const uint32_t bar = full0 + s * 8u;
+            mbar_arrive_expect_tx_remote(bar, C::kStageBytes);
+            tma_load_2d_pair(a_dst, &map_x, bar, k0, r);
+            tma_load_2d_pair(a_dst + C::kBoxBytes, &map_x, bar, k0 + 64, r);
+#pragma unroll
+            for (int i = 0; i < BN / 128; ++i)
+              tma_load_2d_pair(b_dst + i * C::kBoxBytes, &map_dy, bar, n0 + 64 * i, r);
+          }
+          ++c;
+        }
+      }
+      // the even CTA waits for the last copies into every slot (they land in
+      // microseconds); the odd CTA's copies land before the even CTA's MMAs
+      // read them, so before the pair passes the teardown cluster barrier
+      volatile int no_abort = 0;
+      for (uint32_t s = 0; leader && s < S; ++s) {
+        if (c > s) {
+          const uint32_t last = s + S * ((c - 1 - s) / S);
+          mbar_wait(&full[s], (last / S) & 1u, &no_abort, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1 && leader) {
+    constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, 2 * kBM, BN);
+    uint32_t c = 0, t = 0;
+    bool ok = true;
+    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    for (; w.live() && ok; w.next()) {
+      const int r0 = w.r0, r1 = w.r1;
+      if (r1 <= r0) continue;  // empty group: the epilogues write zeros
+      const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty[b], tph ^ 1u, abort_word, lim))) break;
+      tc_fence_after();
+      const uint32_t d = tbase + b * BN;
+      for (int r = r0; r < r1; r += kChunk) {
+        const uint32_t s = c % S, ph = (c / S) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_word, lim))) {
+          ok = false;
+          break;
+        }
+        uint8_t* a_ptr = ring + s * C::kStageBytes;
+        uint8_t* b_ptr = a_ptr + C::kABytes;
+        const int live = r1 - r;
+        const int steps = live < kChunk ? (live + 15) / 16 : 4;
+        if (live < 16 * steps) zero_x_rows(a_ptr, live, 16 * steps, lane);
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(a_ptr);
+          const uint32_t b_addr = smem_u32(b_ptr);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < steps)
+              mma_bf16_pair(d, smem_desc_sw128(a_addr + 2048 * j, C::kBoxBytes, 1024),
+                            smem_desc_sw128(b_addr + 2048 * j, C::kBoxBytes, 1024), idesc,
+                            (r > r0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&empty[s], 0x3);
+        }
+        __syncwarp();
+        ++c;
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit_pair(&tfull[b], 0x3);
+      __syncwarp();
+      ++t;
+    }
+    if (lane == 0 && c > 0) {
+      volatile int no_abort = 0;
+      mma_commit_pair(drain, 0x1);
+      mbar_wait(drain, 0, &no_abort, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // odd CTA: zero the next group's x rows of partial chunks, then count
+    // them on the even CTA's full[s]
+    const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+    uint32_t c = 0, pp = 0;  // pp: parity of ploaded[s], one bit per slot
+    bool ok = true;
+    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    for (; w.live() && ok; w.next()) {
+      for (int r = w.r0; r < w.r1; r += kChunk, ++c) {
+        const int live = w.r1 - r;
+        if (!(live < kChunk && (live & 15) != 0)) continue;
+        const uint32_t s = c % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ploaded[s], (pp >> s) & 1u, abort_word, lim))) {
+          ok = false;
+          break;
+        }
+        pp ^= 1u << s;
+        zero_x_rows(ring + s * C::kStageBytes, live, (live + 15) & ~15, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(full0 + s * 8u);
+      }
+    }
+  } else if (warp >= 2) {
+    const int pw = warp - 2;
+    const int h = pw >> 2;
+    const int quad = warp & 3;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+    uint8_t* box = staging + pw * 4096;
+    uint8_t* brow = box + lane * 128;
+    uint32_t t = 0;
+    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    for (; w.live(); w.next()) {
+      const int g = w.g;
+      const int rem = w.u - g * KPNT;
+      const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128, n0 = (rem % NT) * BN;
+      const int r0 = w.r0, r1 = w.r1;
+      const int y = g * args.K + k0 + quad * 32;
+      uint32_t r[BN / 2];
+      if (r1 <= r0) {
+#pragma unroll
+        for (int j = 0; j < BN / 2; ++j) r[j] = 0u;
+      } else {
+        const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull[b], tph, abort_word, lim))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < BN / 64; ++cc)
+          tmem_ld_32x32(t_lane + b * BN + h * (BN / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * cc));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty0 + b * 8u);
+        ++t;
+      }
+#pragma unroll
+      for (int pass = 0; pass < BN / 128; ++pass) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int cidx = 64 * pass + 8 * j;
+          *reinterpret_cast<uint4*>(brow + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(pack_bf16x2(__uint_as_float(r[cidx]), __uint_as_float(r[cidx + 1])),
+                         pack_bf16x2(__uint_as_float(r[cidx + 2]), __uint_as_float(r[cidx + 3])),
+                         pack_bf16x2(__uint_as_float(r[cidx + 4]), __uint_as_float(r[cidx + 5])),
+                         pack_bf16x2(__uint_as_float(r[cidx + 6]), __uint_as_float(r[cidx + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_dw, box, n0 + h * (BN / 2) + 64 * pass, y);
+          bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+  }
+
+  // teardown: no CTA of the pair leaves while the other may still arrive on
+  // its barriers or its MMAs may still touch the other's TMEM
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, C::kTmemCols);
+  }
+  if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
+}
+
+template <int BN>
+cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
+                        const TgmmArgs& args, int max_pairs, cudaStream_t stream) {
+  constexpr int smem = TgmmPairTile<BN>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(tgmm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // as many pairs as can be resident at once (one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * max_pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, tgmm_pair_kernel<BN>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const int pairs = clusters < max_pairs ? clusters : max_pairs;
+  tgmm_pair_kernel<BN><<<2 * pairs, kThreads, smem, stream>>>(map_x, map_dy, map_dw, args);
+  return cudaGetLastError();
+}
+
 template <int BN>
 cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
                    const TgmmArgs& args, int grid,
@@ -315,6 +637,12 @@ int tgmm_bn(int N) { return (N % 256 == 0) ? 256 : 128; }
 cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
                              const TgmmArgs& args, int grid,
                              cudaStream_t stream) {
+  if (args.K % 256 == 0) {
+    // CTA pairs: grid / 2 pairs at most (grid = min(SMs, tiles))
+    const int max_pairs = grid / 2 > 0 ? grid / 2 : 1;
+    if (args.N % 256 == 0) return launch_pair<256>(map_x, map_dy, map_dw, args, max_pairs, stream);
+    return launch_pair<128>(map_x, map_dy, map_dw, args, max_pairs, stream);
+  }
   if (args.N % 256 == 0) return launch<256>(map_x, map_dy, map_dw, args, grid, stream);
   return launch<128>(map_x, map_dy, map_dw, args, grid, stream);
 }

@@ -17,6 +17,10 @@ EDGE = [
     ([5, 0, 0, 9], 20, 384, 128),
     ([0, 0, 0], 64, 128, 128),
     ([0, 0], 0, 128, 256),
+    # K a multiple of 256: the CTA-pair kernel (256 k rows per pair of CTAs)
+    ([3, 0, 200, 77], 300, 512, 256),
+    ([130, 0, 150], 300, 768, 128),
+    ([0, 0], 0, 256, 256),
 ]
 
 
