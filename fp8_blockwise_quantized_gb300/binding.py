@@ -212,6 +212,16 @@ def _ws(ws, G, M, device):
     return ws
 
 
+def _ws_for(group_sizes, ws, G, M, device):
+    """Workspace of a grouped call.  group_sizes=None reuses the metadata that
+    an earlier call (or group_metadata) left in `ws`, so `ws` must be given."""
+    if group_sizes is None:
+        if ws is None or not ws.fits(G, M):
+            raise ValueError("group_sizes=None reuses the metadata in `workspace`: pass that workspace")
+        return ws
+    return _ws(ws, G, M, device)
+
+
 def quantize_lhs(x: torch.Tensor, stream=None):
     """x bf16 [M, K] -> (xq uint8 [M, K] e4m3 codes, xs float32 [K/128, M])."""
     M, K = x.shape
@@ -237,7 +247,7 @@ def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, s
     N = Nw // 2 if fuse else Nw
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
-    ws_ = _ws(workspace, G, M, xq.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
     _check(gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes,
                        stream), "gmm_fp8_fwd")
     return out
@@ -252,7 +262,7 @@ def fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, with_h=True, workspace=Non
     h = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if with_h else None
     hq = torch.empty((M, N), dtype=torch.uint8, device=xq.device)
     hs = torch.empty((N // 128, M), dtype=torch.float32, device=xq.device)
-    ws_ = _ws(workspace, G, M, xq.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
     _check(gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, ws_.buf, ws_.nbytes,
                                     stream), "gmm_fp8_fwd_swiglu_quant")
     return h, hq, hs
@@ -265,7 +275,7 @@ def bf16_fwd(x, w, group_sizes, fuse=False, out=None, workspace=None, stream=Non
     N = Nw // 2 if fuse else Nw
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    ws_ = _ws(workspace, G, M, x.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, x.device)
     _check(gmm_bf16_fwd(x, w, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes, stream),
            "gmm_bf16_fwd")
     return out
@@ -278,7 +288,7 @@ def dgrad(dy, w, group_sizes, dx=None, workspace=None, stream=None):
     assert N2 == N
     if dx is None:
         dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
-    ws_ = _ws(workspace, G, M, dy.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, dy.device)
     _check(gmm_bf16_dgrad(dy, w, group_sizes, G, M, K, N, dx, ws_.buf, ws_.nbytes, stream), "gmm_bf16_dgrad")
     return dx
 
@@ -287,10 +297,17 @@ def tgmm(x, dy, group_sizes, dw=None, workspace=None, stream=None):
     M, K = x.shape
     M2, N = dy.shape
     assert M2 == M
-    G = group_sizes.numel()
+    if group_sizes is not None:
+        G = group_sizes.numel()
+    elif dw is not None:
+        G = dw.shape[0]
+    elif workspace is not None:
+        G = workspace.G
+    else:
+        raise ValueError("group_sizes=None reuses the metadata in `workspace`: pass that workspace")
     if dw is None:
         dw = torch.empty((G, K, N), dtype=torch.bfloat16, device=x.device)
-    ws_ = _ws(workspace, G, M, x.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, x.device)
     _check(tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, ws_.buf, ws_.nbytes, stream), "tgmm_bf16")
     return dw
 

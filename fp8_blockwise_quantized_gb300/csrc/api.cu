@@ -214,7 +214,7 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
   const int64_t Nw = fuse ? 2 * N : N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
-  if (!wq || !ws || !group_sizes) return GMM_ERR_NULL;
+  if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !out)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(out) ||
       !aligned16(group_sizes))
@@ -223,7 +223,7 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse);
@@ -255,7 +255,7 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   const int64_t Nw = 2 * N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
-  if (!wq || !ws || !group_sizes) return GMM_ERR_NULL;
+  if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !hq || !hs)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(h) || !aligned16(hq) ||
       !aligned16(hs) || !aligned16(group_sizes))
@@ -264,7 +264,7 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), 1);
@@ -305,14 +305,14 @@ gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes
   const int64_t Nw = fuse ? 2 * N : N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
-  if (!w || !group_sizes) return GMM_ERR_NULL;
+  if (!w) return GMM_ERR_NULL;
   if (M > 0 && (!x || !out)) return GMM_ERR_NULL;
   if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned16(group_sizes)) return GMM_ERR_ALIGN;
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = bf16_geometry(static_cast<int>(N), fuse);
@@ -340,14 +340,14 @@ gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_si
   // reduction is N and whose output columns are K
   gmm_status st = check_grouped(G, M, N, K, K);
   if (st != GMM_OK) return st;
-  if (!w || !group_sizes) return GMM_ERR_NULL;
+  if (!w) return GMM_ERR_NULL;
   if (M > 0 && (!dy || !dx)) return GMM_ERR_NULL;
   if (!aligned16(dy) || !aligned16(w) || !aligned16(dx) || !aligned16(group_sizes)) return GMM_ERR_ALIGN;
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
 
   const int bn = (K % 256 == 0) ? 256 : 128;
@@ -377,14 +377,14 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
   if (st != GMM_OK) return st;
   // the kernel walks its output tiles with 32-bit indices
   if (static_cast<int64_t>(G) * (K / 128) * (N / tgmm_bn(static_cast<int>(N))) > INT32_MAX / 2) return GMM_ERR_SHAPE;
-  if (!dw || !group_sizes) return GMM_ERR_NULL;
+  if (!dw) return GMM_ERR_NULL;
   if (M > 0 && (!x || !dy)) return GMM_ERR_NULL;
   if (!aligned16(x) || !aligned16(dy) || !aligned16(dw) || !aligned16(group_sizes)) return GMM_ERR_ALIGN;
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
 
   // With M == 0 every group is empty: the kernel only writes zeros and never
   // reads x or dy, so the maps may describe a dummy one-row tensor.

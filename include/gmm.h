@@ -27,6 +27,12 @@
  *   - Row-major layouts; bf16 = IEEE bfloat16; e4m3 = OCP FP8 E4M3 (max 448).
  *   - K and N are multiples of 128 (the quantization block); 1 <= G <= 4096;
  *     0 <= M < 2^31.  M = 0, or every group empty, is valid.
+ *   - The grouped calls first derive the group metadata (offsets, row tiles)
+ *     from group_sizes into the workspace.  group_sizes = NULL skips that step
+ *     and reuses the metadata already in the workspace: written by
+ *     gmm_group_metadata or by an earlier grouped call with the same G and M,
+ *     enqueued earlier on the same stream (the layers of one MoE block share
+ *     their routing, so one metadata pass serves all their grouped calls).
  */
 #ifndef GMM_GB300_H
 #define GMM_GB300_H
@@ -79,8 +85,9 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
  *                  every group cut into consecutive tiles of at most 128 rows,
  *                  groups in order, empty groups contributing none.
- * The grouped calls below run this step themselves; it is exported so that
- * it can be checked and timed on its own.
+ * The grouped calls below run this step themselves unless they are given
+ * group_sizes = NULL, in which case they read what this call (or an earlier
+ * grouped call) left in the workspace.
  */
 gmm_status gmm_group_metadata(const int32_t* group_sizes, int G, int64_t M, void* workspace,
                               size_t workspace_bytes, void* stream);

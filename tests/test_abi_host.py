@@ -76,12 +76,20 @@ def _fp8(lib, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(K=100), 2), (dict(N=0), 2), (dict(G=0), 2), (dict(G=5000), 2), (dict(M=-1), 2),
-    (dict(M=1 << 31), 2), (dict(wq=None), 1), (dict(gs=None), 1), (dict(out=None), 1),
+    (dict(M=1 << 31), 2), (dict(wq=None), 1), (dict(out=None), 1), (dict(gs=FAKE + 4), 3),
     (dict(xq=FAKE + 8), 3), (dict(out=FAKE + 2), 3), (dict(work=None), 8), (dict(wbytes=16), 8),
     (dict(work=FAKE + 4), 3),
 ])
 def test_fp8_host_validation(lib, kw, code):
     assert _fp8(lib, **kw) == code
+
+
+def test_null_group_sizes_is_not_a_host_error(lib):
+    # group_sizes = NULL reuses the workspace's metadata: shape errors are still
+    # reported first, and a missing weight is still a null-pointer error
+    assert _fp8(lib, gs=None, K=100) == 2
+    assert _fp8(lib, gs=None, wq=None) == 1
+    assert lib.tgmm_bf16(FAKE, FAKE, None, 4, 512, 256, 256, None, FAKE, 1 << 20, None) == 1
 
 
 def test_host_validation_other_calls(lib):
