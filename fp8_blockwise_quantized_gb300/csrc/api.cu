@@ -121,8 +121,8 @@ gmm_status check_grouped(int G, int64_t M, int64_t K, int64_t N, int64_t Nw) {
 gmm_status launch_metadata(const int32_t* sizes, int G, int64_t M, void* workspace, cudaStream_t st) {
   int32_t* ws = static_cast<int32_t*>(workspace);
   Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(workspace) + tiles_offset_bytes(G));
-  group_metadata_kernel<<<1, 1024, 0, st>>>(sizes, G, static_cast<int>(M), ws, tiles);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, st, sizes, G, static_cast<int>(M), ws,
+                             tiles);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "group_metadata_kernel launch");
 }
 
@@ -184,10 +184,9 @@ gmm_status gmm_quantize_lhs(const void* x, int64_t M, int64_t K, void* xq, float
   const long long per_cta = 8LL * kLhsBlocksPerWarp;  // 8 warps per CTA
   long long grid = (nblocks + per_cta - 1) / per_cta;
   if (grid > static_cast<long long>(di.sms) * 8) grid = static_cast<long long>(di.sms) * 8;
-  quantize_lhs_kernel<<<static_cast<int>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(x), static_cast<int>(M), static_cast<int>(K / 128), nblocks, static_cast<uint2*>(xq),
-      xs);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(quantize_lhs_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                             static_cast<cudaStream_t>(stream), static_cast<const uint4*>(x), static_cast<int>(M),
+                             static_cast<int>(K / 128), nblocks, static_cast<uint2*>(xq), xs);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "quantize_lhs_kernel launch");
 }
 

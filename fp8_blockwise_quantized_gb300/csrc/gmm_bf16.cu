@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();  // inputs and metadata come from earlier kernels
 
   const int num_tiles = args.meta[kWsNumTiles];
   const int units_per_tile = args.N / C::kOutCols;
@@ -271,8 +273,7 @@ cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const Fwd
   cudaError_t e =
       cudaFuncSetAttribute(gmm_bf16_kernel<BN, FUSE, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gmm_bf16_kernel<BN, FUSE, BK><<<grid, kThreads, smem, stream>>>(map_a, map_b, args);
-  return cudaGetLastError();
+  return launch_pdl(gmm_bf16_kernel<BN, FUSE, BK>, dim3(grid), dim3(kThreads), smem, stream, map_a, map_b, args);
 }
 
 }  // namespace

@@ -169,6 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();  // inputs and metadata come from earlier kernels
 
   const int num_tiles = args.meta[kWsNumTiles];
   const int units_per_tile = args.N / C::kOutCols;
@@ -529,8 +531,8 @@ cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUt
   cudaError_t e =
       cudaFuncSetAttribute(gmm_fp8_kernel<BN, FUSE, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  gmm_fp8_kernel<BN, FUSE, QUANT><<<grid, kThreads, smem, stream>>>(map_a, map_b, map_out, args);
-  return cudaGetLastError();
+  return launch_pdl(gmm_fp8_kernel<BN, FUSE, QUANT>, dim3(grid), dim3(kThreads), smem, stream, map_a, map_b,
+                    map_out, args);
 }
 
 }  // namespace

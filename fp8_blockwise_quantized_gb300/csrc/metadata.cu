@@ -10,6 +10,7 @@
 // every thread then writes its groups' offsets and 128-row tiles.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace gmm {
 
@@ -52,6 +53,8 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
                                                                 int M, int32_t* __restrict__ ws,
                                                                 Tile* __restrict__ tiles) {
   __shared__ long long warp_sums[33];
+  griddep_launch_dependents();
+  griddep_wait();  // group_sizes may come from the previous kernel
   const int t = threadIdx.x;
   const int per = (G + 1023) / 1024;
   const int g0 = min(G, t * per), g1 = min(G, g0 + per);

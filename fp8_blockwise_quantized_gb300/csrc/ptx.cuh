@@ -22,6 +22,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: launch_dependents lets the next kernel on the
+// stream start its CTAs on SMs that free up; they run their set-up and then
+// wait in griddep_wait until this grid has completed and its memory
+// operations are visible.  Every kernel here reads its inputs only after
+// griddep_wait (and it returns at once when there is no such dependency).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

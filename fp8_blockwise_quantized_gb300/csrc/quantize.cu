@@ -10,6 +10,7 @@
 // codes and scales are bit-identical to any correct fp32 implementation.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace gmm {
 
@@ -35,6 +36,8 @@ __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restri
                                                            long long nblocks, uint2* __restrict__ xq,
                                                            float* __restrict__ xs) {
   constexpr int kPerHalf = kLhsBlocksPerWarp / 2;
+  griddep_launch_dependents();
+  griddep_wait();  // x may come from the previous kernel
   const int lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();  // inputs and metadata come from earlier kernels
 
   const bool valid_meta = args.meta[kWsValid] != 0;
   const int KT = args.K / 128, NT = args.N / BN, KTNT = KT * NT;
@@ -393,6 +395,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();  // inputs and metadata come from earlier kernels
 
   const bool valid_meta = args.meta[kWsValid] != 0;
   const int KP = args.K / 256, NT = args.N / BN, KPNT = KP * NT;
@@ -615,8 +619,8 @@ cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, con
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const int pairs = clusters < max_pairs ? clusters : max_pairs;
-  tgmm_pair_kernel<BN><<<2 * pairs, kThreads, smem, stream>>>(map_x, map_dy, map_dw, args);
-  return cudaGetLastError();
+  return launch_pdl(tgmm_pair_kernel<BN>, dim3(2 * pairs), dim3(kThreads), smem, stream, map_x, map_dy, map_dw,
+                    args);
 }
 
 template <int BN>
@@ -626,8 +630,7 @@ cudaError_t launch(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CU
   constexpr int smem = TgmmTile<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(tgmm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tgmm_kernel<BN><<<grid, kThreads, smem, stream>>>(map_x, map_dy, map_dw, args);
-  return cudaGetLastError();
+  return launch_pdl(tgmm_kernel<BN>, dim3(grid), dim3(kThreads), smem, stream, map_x, map_dy, map_dw, args);
 }
 
 }  // namespace
