@@ -177,8 +177,8 @@ def accounting(sizes: np.ndarray):
 # was taken on: the SHA-256 of that .cu file is checked at run time and the
 # traffic is reported as null once the kernel has changed.
 MEASURED_TRAFFIC = {
-    "tgmm_wi": {"bytes": 552059136 + 1021028096, "source": "tgmm.cu",
-                "sha256": "450d1560beb8658593fa7989a5d8320b1c52a040368bfdcbaf7d34fc0cd63109"},
+    "tgmm_wi": {"bytes": 549666816 + 1019843584, "source": "tgmm.cu",
+                "sha256": "1c4815b2c4d7461cbe62eea383cbf083b4dd764eecca0b450bfb3f7d5a7b7bdf"},
 }
 
 
