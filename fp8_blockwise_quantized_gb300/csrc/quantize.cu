@@ -27,15 +27,18 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 }  // namespace
 
-// LHS, 1x128 blocks.  X is row-major [M, K] with K % 128 == 0, so block b =
-// (m, kb) occupies bytes [256 b, 256 b + 256) of X: the blocks form one
-// linear sequence.  A half-warp (16 lanes x 16 bytes) handles one block; a
-// warp handles kLhsBlocksPerWarp consecutive blocks per step, all loads issued
-// before any reduction, for memory-level parallelism.
+// LHS, 1x128 blocks.  X is row-major [M, K] with K % 128 == 0; block (m, kb)
+// occupies bytes [256 (m KB + kb), + 256) of X.  A half-warp (16 lanes x 16
+// bytes) handles one block; a warp handles the blocks kb of eight consecutive
+// rows per step (slots in groups of 8 rows), all loads issued before any
+// reduction, for memory-level parallelism, so that its eight scales are one
+// contiguous 32-byte run of xs[kb][m] instead of eight scattered words.
 __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restrict__ x, int M, int KB,
                                                            long long nblocks, uint2* __restrict__ xq,
                                                            float* __restrict__ xs) {
   constexpr int kPerHalf = kLhsBlocksPerWarp / 2;
+  static_assert(kLhsBlocksPerWarp == 8, "a warp step covers eight rows");
+  (void)nblocks;
   griddep_launch_dependents();
   griddep_wait();  // x may come from the previous kernel
   const int lane = threadIdx.x & 31;
@@ -43,16 +46,21 @@ __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restri
   const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
 
-  for (long long base = warp_id * kLhsBlocksPerWarp; base < nblocks; base += nwarps * kLhsBlocksPerWarp) {
+  const long long nslots = ((M + 7) / 8) * 8LL * KB;
+  for (long long base = warp_id * kLhsBlocksPerWarp; base < nslots; base += nwarps * kLhsBlocksPerWarp) {
     uint4 v[kPerHalf];
+    const long long grp = base >> 3;
+    const long long mg = grp / KB, kbg = grp - mg * KB;
 #pragma unroll
     for (int i = 0; i < kPerHalf; ++i) {
-      const long long b = base + half * kPerHalf + i;
-      v[i] = (b < nblocks) ? __ldcs(x + b * 16 + l16) : make_uint4(0, 0, 0, 0);
+      const long long m = mg * 8 + half * kPerHalf + i;
+      const long long b = m * KB + kbg;
+      v[i] = (m < M) ? __ldcs(x + b * 16 + l16) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kPerHalf; ++i) {
-      const long long b = base + half * kPerHalf + i;
+      const long long m = mg * 8 + half * kPerHalf + i;
+      const long long b = m * KB + kbg;
       float f[8];
       bf16x8_to_f32(v[i], f);
       float amax = 0.0f;
@@ -67,13 +75,9 @@ __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restri
             (e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16);
       q.y = e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
             (e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16);
-      if (b < nblocks) {
+      if (m < M) {
         xq[b * 16 + l16] = q;
-        if (l16 == 0) {
-          const long long m = b / KB;
-          const long long kb = b - m * KB;
-          xs[kb * M + m] = s;
-        }
+        if (l16 == 0) xs[kbg * M + m] = s;
       }
     }
   }
