@@ -338,6 +338,8 @@ def run_gpu(args):
             per_kernel[n].append(ev[j].elapsed_time(ev[j + 1]))
     ms = float(np.mean(step_ms))
     total_ms = float(np.sum(step_ms))
+    step_dist = {"median": round(float(np.median(step_ms)), 4), "p10": round(float(np.percentile(step_ms, 10)), 4),
+                 "p90": round(float(np.percentile(step_ms, 90)), 4)}
     if ws_ > 1:
         total_ms = max_over_ranks(total_ms, dev)
         ms = total_ms / args.steps
@@ -477,7 +479,7 @@ def run_gpu(args):
         return None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "step_ms": step_dist, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 MMA + bf16 MMA, fp32 accumulate",
         "data": "synthetic (seeded; routing Zipf(1.1) top-8; X N(0,1) with 1% x50 outliers)",
         "config": {"workload": WORKLOAD, "G": G, "M": M, "K": K, "N": N, "step_gflop": round(step_flops / 1e9, 2),
