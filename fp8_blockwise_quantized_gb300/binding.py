@@ -205,6 +205,11 @@ class Workspace:
         off = gmm_tiles_offset(self.G)
         return self.buf[off:off + 16 * n].view(torch.int32).view(n, 4)[:, :3]
 
+    def order(self) -> list[int]:
+        """The group ids sorted by size, largest first (ties by id)."""
+        off = gmm_tiles_offset(self.G) + 16 * ((self.M + 127) // 128 + self.G)
+        return self.buf[off:off + 4 * self.G].view(torch.int32).tolist()
+
 
 def _ws(ws, G, M, device):
     if ws is None or not ws.fits(G, M):

@@ -121,8 +121,9 @@ gmm_status check_grouped(int G, int64_t M, int64_t K, int64_t N, int64_t Nw) {
 gmm_status launch_metadata(const int32_t* sizes, int G, int64_t M, void* workspace, cudaStream_t st) {
   int32_t* ws = static_cast<int32_t*>(workspace);
   Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(workspace) + tiles_offset_bytes(G));
+  int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + order_offset_bytes(G, M));
   cudaError_t e = launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, st, sizes, G, static_cast<int>(M), ws,
-                             tiles);
+                             tiles, order);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "group_metadata_kernel launch");
 }
 
@@ -398,6 +399,7 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
     return st;
   TgmmArgs a{};
   a.meta = static_cast<const int32_t*>(workspace);
+  a.order = reinterpret_cast<const int32_t*>(static_cast<const char*>(workspace) + order_offset_bytes(G, M));
   a.dw = static_cast<uint16_t*>(dw);
   a.G = G;
   a.M = static_cast<int>(M);

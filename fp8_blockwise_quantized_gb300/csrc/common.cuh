@@ -29,8 +29,12 @@ __host__ __device__ inline int64_t tiles_capacity(int G, int64_t M) { return (M 
 __host__ __device__ inline int64_t tiles_offset_bytes(int G) {
   return ((static_cast<int64_t>(kWsOffsets + G + 1) * 4 + 15) / 16) * 16;
 }
-__host__ __device__ inline int64_t workspace_bytes(int G, int64_t M) {
+// the groups ordered by size (descending, ties by index) follow the tiles
+__host__ __device__ inline int64_t order_offset_bytes(int G, int64_t M) {
   return tiles_offset_bytes(G) + 16 * tiles_capacity(G, M);
+}
+__host__ __device__ inline int64_t workspace_bytes(int G, int64_t M) {
+  return order_offset_bytes(G, M) + ((4 * static_cast<int64_t>(G) + 15) / 16) * 16;
 }
 
 // Bounded-wait limit handed to every kernel (nanoseconds of %globaltimer).

@@ -30,7 +30,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // ---- a1 metadata ------------------------------------------------------------
-__global__ void group_metadata_kernel(const int32_t* sizes, int G, int M, int32_t* ws, Tile* tiles);
+__global__ void group_metadata_kernel(const int32_t* sizes, int G, int M, int32_t* ws, Tile* tiles,
+                                      int32_t* order);
 
 // ---- a2 / a3 quantization -----------------------------------------------------
 constexpr int kLhsBlocksPerWarp = 8;
@@ -54,6 +55,7 @@ struct FwdArgs {
 
 struct TgmmArgs {
   const int32_t* meta;    // workspace words (offsets)
+  const int32_t* order;   // workspace: groups by size, descending
   uint16_t* dw;           // bf16 [G][K][N]
   int G, M, K, N;
   uint64_t wait_limit_ns;

@@ -51,8 +51,10 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 
 __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __restrict__ sizes, int G,
                                                                 int M, int32_t* __restrict__ ws,
-                                                                Tile* __restrict__ tiles) {
+                                                                Tile* __restrict__ tiles,
+                                                                int32_t* __restrict__ order) {
   __shared__ long long warp_sums[33];
+  __shared__ unsigned long long keys[kMaxGroups];
   griddep_launch_dependents();
   griddep_wait();  // group_sizes may come from the previous kernel
   const int t = threadIdx.x;
@@ -94,6 +96,33 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
       }
       off += n;
     }
+  }
+  if (err == 0) {
+    // the groups by size, descending, ties by index (a bitonic sort of
+    // (INT32_MAX - size, g) keys): the tgmm kernels deal the units of the
+    // largest groups first, so that the last units of the grid are small
+    int P = 1;
+    while (P < G) P <<= 1;
+    for (int i = t; i < P; i += blockDim.x)
+      keys[i] = i < G ? (static_cast<unsigned long long>(0x7fffffff - sizes[i]) << 32) | static_cast<unsigned>(i)
+                      : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = t; i < P; i += blockDim.x) {
+          const int l = i ^ j;
+          if (l > i) {
+            const unsigned long long a = keys[i], b = keys[l];
+            if ((a > b) == ((i & k) == 0)) {
+              keys[i] = b;
+              keys[l] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (int i = t; i < G; i += blockDim.x) order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
   }
   if (t == 0) {
     if (err) {

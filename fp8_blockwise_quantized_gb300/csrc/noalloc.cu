@@ -123,8 +123,9 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   int32_t* meta = static_cast<int32_t*>(d.scratch);
   if (cudaMemsetAsync(meta + kWsStatus, 0, sizeof(int32_t), s) != cudaSuccess) return GMM_ERR_CUDA;
   Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(d.scratch) + tiles_offset_bytes(G));
+  int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(d.scratch) + order_offset_bytes(G, M));
   if (launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, s, group_sizes, G, static_cast<int>(M), meta,
-                 tiles) != cudaSuccess)
+                 tiles, order) != cudaSuccess)
     return GMM_ERR_CUDA;
   if (M == 0) return GMM_OK;
 

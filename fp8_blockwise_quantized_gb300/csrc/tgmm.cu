@@ -35,17 +35,28 @@ constexpr int kEpiWarps = 8;
 constexpr int kChunk = 64;  // rows per stage
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-// This CTA's units u = first, first + stride, ... (u / per_group is the
-// group).  The next unit's group offsets are loaded one unit ahead, so their
-// global-memory latency overlaps the current unit instead of sitting between
-// two units on each role's critical path.
+// The units of a launch are numbered group by group, the groups taken
+// largest first (`order`: the groups by size, descending), and dealt to the
+// CTAs (or CTA pairs) in snake order: round r gives unit r * stride + first
+// when r is even and r * stride + stride - 1 - first when it is odd.  The big
+// units come first and each CTA's rounds alternate ends, so the last wave
+// holds small units and the loads stay balanced.  Unit u covers group
+// order[u / per_group], column/row block u % per_group.  The next unit's group
+// and offsets are loaded one unit ahead, so their global-memory latency
+// overlaps the current unit.
 struct UnitWalk {
   const int* offsets;
-  int per_group, num, step, u, g, r0, r1, gn, r0n, r1n;
-  __device__ UnitWalk(const int* off, int per_group_units, int num_units, int first, int stride)
-      : offsets(off), per_group(per_group_units), num(num_units), step(stride), u(first), g(0), r0(0), r1(0) {
+  const int* order;
+  int per_group, num, step, first, round, u, g, rem, r0, r1, un, gn, r0n, r1n;
+  __device__ int unit_of(int r) const { return r * step + ((r & 1) ? step - 1 - first : first); }
+  __device__ UnitWalk(const int* off, const int* ord, int per_group_units, int num_units, int first_unit,
+                      int stride)
+      : offsets(off), order(ord), per_group(per_group_units), num(num_units), step(stride), first(first_unit),
+        round(0), g(0), rem(0), r0(0), r1(0) {
+    u = unit_of(0);
     if (u < num) {
-      g = u / per_group;
+      g = __ldg(order + u / per_group);
+      rem = u % per_group;
       r0 = __ldg(offsets + g);
       r1 = __ldg(offsets + g + 1);
     }
@@ -53,18 +64,20 @@ struct UnitWalk {
   }
   __device__ bool live() const { return u < num; }
   __device__ void prefetch() {
-    const int un = u + step;
+    un = unit_of(round + 1);
     gn = 0;
     r0n = r1n = 0;
     if (un < num) {
-      gn = un / per_group;
+      gn = __ldg(order + un / per_group);
       r0n = __ldg(offsets + gn);
       r1n = __ldg(offsets + gn + 1);
     }
   }
   __device__ void next() {
-    u += step;
+    ++round;
+    u = un;
     g = gn;
+    rem = u % per_group;
     r0 = r0n;
     r1 = r1n;
     prefetch();
@@ -142,9 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
+      UnitWalk w(offsets, args.order, KTNT, num_units, blockIdx.x, gridDim.x);
       for (; w.live() && ok; w.next()) {
-        const int rem = w.u - w.g * KTNT;
+        const int rem = w.rem;
         const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
         const int r0 = w.r0, r1 = w.r1;
         for (int r = r0; r < r1; r += kChunk) {
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, kBM, BN);
     uint32_t c = 0, t = 0;
     bool ok = true;
-    UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
+    UnitWalk w(offsets, args.order, KTNT, num_units, blockIdx.x, gridDim.x);
     for (; w.live() && ok; w.next()) {
       const int r0 = w.r0, r1 = w.r1;
       if (r1 <= r0) continue;  // empty group: the epilogue writes zeros
@@ -240,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* box = staging + pw * 4096;
     uint8_t* brow = box + lane * 128;  // this thread's row of the box
     uint32_t t = 0;
-    UnitWalk w(offsets, KTNT, num_units, blockIdx.x, gridDim.x);
+    UnitWalk w(offsets, args.order, KTNT, num_units, blockIdx.x, gridDim.x);
     for (; w.live(); w.next()) {
       const int g = w.g;
-      const int rem = w.u - g * KTNT;
+      const int rem = w.rem;
       const int k0 = (rem / NT) * 128, n0 = (rem % NT) * BN;
       const int r0 = w.r0, r1 = w.r1;
       const int y = g * args.K + k0 + quad * 32;
@@ -410,9 +423,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
       uint32_t c = 0;
       bool ok = true;
-      UnitWalk w(offsets, KPNT, num_units, first, stride);
+      UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
       for (; w.live() && ok; w.next()) {
-        const int rem = w.u - w.g * KPNT;
+        const int rem = w.rem;
         const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128;
         const int n0 = (rem % NT) * BN + static_cast<int>(rank) * (BN / 2);
         for (int r = w.r0; r < w.r1; r += kChunk) {
@@ -464,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, 2 * kBM, BN);
     uint32_t c = 0, t = 0;
     bool ok = true;
-    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
     for (; w.live() && ok; w.next()) {
       const int r0 = w.r0, r1 = w.r1;
       if (r1 <= r0) continue;  // empty group: the epilogues write zeros
@@ -517,7 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);
     uint32_t c = 0, pp = 0;  // pp: parity of ploaded[s], one bit per slot
     bool ok = true;
-    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
     for (; w.live() && ok; w.next()) {
       for (int r = w.r0; r < w.r1; r += kChunk, ++c) {
         const int live = w.r1 - r;
@@ -542,10 +555,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* box = staging + pw * 4096;
     uint8_t* brow = box + lane * 128;
     uint32_t t = 0;
-    UnitWalk w(offsets, KPNT, num_units, first, stride);
+    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
     for (; w.live(); w.next()) {
       const int g = w.g;
-      const int rem = w.u - g * KPNT;
+      const int rem = w.rem;
       const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128, n0 = (rem % NT) * BN;
       const int r0 = w.r0, r1 = w.r1;
       const int y = g * args.K + k0 + quad * 32;

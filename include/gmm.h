@@ -64,9 +64,9 @@ const char* gmm_last_cuda_error(void);
 
 /*
  * Bytes of device workspace the grouped calls need for G groups and M rows:
- * a status word, the group offsets and the row-tile list.  The workspace must
- * be zero-filled once before its first use (its first word is the sticky
- * error word); afterwards it may be reused by any number of calls issued on
+ * a status word, the group offsets, the row-tile list and the groups ordered
+ * by size.  The workspace must be zero-filled once before its first use (its
+ * first word is the sticky error word); afterwards it may be reused by any number of calls issued on
  * one stream.  Two calls that run concurrently need two workspaces.
  */
 size_t gmm_workspace_bytes(int G, int64_t M);
@@ -85,6 +85,9 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
  *                  every group cut into consecutive tiles of at most 128 rows,
  *                  groups in order, empty groups contributing none.
+ *   int32 order[G] at byte offset gmm_tiles_offset(G) + 16 * (ceil(M/128) + G):
+ *                  the group ids sorted by size, largest first (ties by id);
+ *                  the tgmm kernels deal their work largest groups first.
  * The grouped calls below run this step themselves unless they are given
  * group_sizes = NULL, in which case they read what this call (or an earlier
  * grouped call) left in the workspace.

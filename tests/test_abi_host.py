@@ -59,7 +59,7 @@ def test_workspace_size(lib):
         assert n >= 32 + 4 * (G + 1) + 16 * tiles
         off = lib.gmm_tiles_offset(G)
         assert off % 16 == 0 and off >= 32 + 4 * (G + 1)
-        assert n == off + 16 * tiles
+        assert n == off + 16 * tiles + (4 * G + 15) // 16 * 16  # + the size-ordered group ids
     assert lib.gmm_workspace_bytes(0, 10) == 0
 
 

@@ -30,6 +30,9 @@ def test_offsets_and_tiles(sizes, M):
     assert hdr[2] == off[-1] and hdr[3] == len(tiles)
     assert ws.offsets() == off.tolist()
     assert np.array_equal(ws.tiles().cpu().numpy(), tiles.astype(np.int32))
+    # the group ids by size, largest first, ties by id (numpy's stable sort)
+    sz = np.asarray(sizes, np.int64)
+    assert ws.order() == np.argsort(-sz, kind="stable").tolist()
     assert gmm.gmm_get_device_status(ws.buf) == 0
 
 
