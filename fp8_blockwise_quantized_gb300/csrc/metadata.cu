@@ -98,31 +98,20 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
     }
   }
   if (err == 0) {
-    // the groups by size, descending, ties by index (a bitonic sort of
-    // (INT32_MAX - size, g) keys): the tgmm kernels deal the units of the
-    // largest groups first, so that the last units of the grid are small
-    int P = 1;
-    while (P < G) P <<= 1;
-    for (int i = t; i < P; i += blockDim.x)
-      keys[i] = i < G ? (static_cast<unsigned long long>(0x7fffffff - sizes[i]) << 32) | static_cast<unsigned>(i)
-                      : ~0ull;
+    // the groups by size, descending, ties by index: group g's place is the
+    // number of keys (INT32_MAX - size, index) below its own (all keys are
+    // distinct), so each thread ranks its groups against all G keys, read as
+    // shared-memory broadcasts.  The tgmm kernels deal the units of the
+    // largest groups first, so that the last units of the grid are small.
+    for (int i = t; i < G; i += blockDim.x)
+      keys[i] = (static_cast<unsigned long long>(0x7fffffff - sizes[i]) << 32) | static_cast<unsigned>(i);
     __syncthreads();
-    for (int k = 2; k <= P; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = t; i < P; i += blockDim.x) {
-          const int l = i ^ j;
-          if (l > i) {
-            const unsigned long long a = keys[i], b = keys[l];
-            if ((a > b) == ((i & k) == 0)) {
-              keys[i] = b;
-              keys[l] = a;
-            }
-          }
-        }
-        __syncthreads();
-      }
+    for (int i = t; i < G; i += blockDim.x) {
+      const unsigned long long mine = keys[i];
+      int rank = 0;
+      for (int j = 0; j < G; ++j) rank += keys[j] < mine ? 1 : 0;
+      order[rank] = i;
     }
-    for (int i = t; i < G; i += blockDim.x) order[i] = static_cast<int32_t>(keys[i] & 0xffffffffu);
   }
   if (t == 0) {
     if (err) {
