@@ -18,6 +18,10 @@ constexpr int kWsStatus = 0;
 constexpr int kWsValid = 1;
 constexpr int kWsS = 2;
 constexpr int kWsNumTiles = 3;
+// Work counters of the CTA-pair tgmm kernel: units claimed, and CTAs that have
+// finished (the last one resets both to zero for the next launch).
+constexpr int kWsClaimed = 4;
+constexpr int kWsFinished = 5;
 constexpr int kWsOffsets = 8;
 
 // Row tile height of every grouped kernel (the tcgen05 MMA M).

@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
     }
   }
   if (t == 0) {
+    ws[kWsClaimed] = 0;
+    ws[kWsFinished] = 0;
     if (err) {
       atomicOr(ws + kWsStatus, err);
       ws[kWsValid] = 0;

@@ -111,6 +111,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_ad
   asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(bytes)
                : "memory");
 }
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to shared memory of a CTA of the cluster, counted
+// on an mbarrier there (cluster addresses `dst_cluster`, `bar_cluster`).  The
+// data is visible to a thread of that CTA once it has seen the barrier phase
+// complete; the source must have been fenced into the async proxy.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                    uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
 // Tiled load into this CTA's shared memory whose completion is counted on an
 // mbarrier of either CTA of the pair (cluster address `bar_cluster`).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster,

@@ -333,7 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 //              full[s].
 //   warps 2-9  epilogue (each CTA, its 128 k rows); the odd CTA's warps free
 //              the pair's TMEM buffer by remote arrives on the even CTA.
+//   warp 10    even CTA: the pair's scheduler (below).
+// Scheduling: the units are numbered largest groups first and the pairs
+// claim them from a counter in the workspace as they go (list scheduling in
+// decreasing size), so a pair that runs slower, or drew larger units, takes
+// fewer.  The scheduler claims a few units ahead of the producer (one claim
+// in flight while the previous one is resolved, several small units per claim
+// once the units get small) and puts each unit {g, rem, r0, r1} in a queue of kQueue entries in
+// its own shared memory and, by a bulk copy that completes on the odd CTA's
+// barrier, in the odd CTA's.  Every role of both CTAs takes the units from
+// its queue in the same order and frees an entry on the even CTA once it has
+// read it.  The last CTA to finish resets the counters for the next launch.
 constexpr int kPairStages = 6;
+constexpr int kPairThreads = 352;
+constexpr int kSchedWarp = 10;
+constexpr int kQueue = 16;
+constexpr int kQueueReaders = 2 * (2 + kEpiWarps);  // producer, warp 1, epilogue warps; both CTAs
+constexpr int kClaimAhead = 3;  // units claimed beyond those the even CTA's producer has taken
 
 // Zero rows [from, to) of both 64-row x boxes of a ring slot (128 bytes per
 // row and box, so the swizzle does not matter) and fence them into the async
@@ -357,11 +373,41 @@ struct TgmmPairTile {
   static constexpr int kStages = BN == 256 ? kPairStages : 8;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kStagingBytes = kEpiWarps * 4096;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 512;
+  // queue entries (16 bytes each), then the barriers, the TMEM address and the abort word
+  static constexpr int kTailBytes = 16 * kQueue + 8 * (3 * kStages + 5 + 2 * kQueue) + 12;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 1024;
+  static_assert(kTailBytes <= 1024, "barrier area");
+};
+
+// Entry i of a CTA's unit queue (every lane of the calling warp, or the one
+// thread of a single-thread role, with `warp_wide` false); the entry is freed
+// on the even CTA as soon as it has been read.
+struct UnitQueue {
+  uint64_t* full;
+  uint64_t* empty;
+  const int4* data;
+  uint32_t empty_leader;  // shared::cluster address of the even CTA's empty[0]
+  bool leader;
+  __device__ bool get(uint32_t i, int4& e, bool warp_wide, int lane, volatile int* abort_word,
+                      uint64_t lim) const {
+    const uint32_t slot = i % kQueue, ph = (i / kQueue) & 1u;
+    bool ok = mbar_wait(&full[slot], ph, abort_word, lim);
+    if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    e = data[slot];
+    if (warp_wide) __syncwarp();
+    if (lane == 0) {
+      if (leader)
+        mbar_arrive(&empty[slot]);
+      else
+        mbar_arrive_remote(empty_leader + slot * 8u);
+    }
+    return true;
+  }
 };
 
 template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tgmm_pair_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dy,
                      const __grid_constant__ CUtensorMap map_dw, const TgmmArgs args) {
   using C = TgmmPairTile<BN>;
@@ -370,19 +416,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
   uint8_t* staging = smem + S * C::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::kStagingBytes);  // even CTA: both halves ready
+  int4* qdata = reinterpret_cast<int4*>(staging + C::kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(qdata + kQueue);  // even CTA: both halves ready
   uint64_t* ploaded = full + S;  // odd CTA: a chunk to be zeroed landed
   uint64_t* empty = ploaded + S;
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;      // even CTA: both CTAs' epilogues freed buffer b
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* qfull = drain + 1;       // each CTA: queue entry written
+  uint64_t* qempty = qfull + kQueue;  // even CTA: every reader of both CTAs has read the entry
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + kQueue);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* taken = abort_word + 1;  // even CTA: queue entries its producer has taken
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
+    *taken = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 2);
       mbar_init(&ploaded[s], 1);
@@ -393,6 +444,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[b], 2 * kEpiWarps);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < kQueue; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], kQueueReaders);
+    }
     *abort_word = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_x);
@@ -409,26 +464,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   griddep_launch_dependents();
-  griddep_wait();  // inputs and metadata come from earlier kernels
+  griddep_wait();  // inputs, metadata and the work counter come from earlier kernels
 
   const bool valid_meta = args.meta[kWsValid] != 0;
   const int KP = args.K / 256, NT = args.N / BN, KPNT = KP * NT;
   const int num_units = valid_meta ? args.G * KPNT : 0;
-  const int first = static_cast<int>(blockIdx.x >> 1), stride = static_cast<int>(gridDim.x >> 1);
   const int* offsets = args.meta + kWsOffsets;
   const uint64_t lim = args.wait_limit_ns;
+  const UnitQueue queue{qfull, qempty, qdata, mapa_shared(smem_u32(qempty), 0), leader};
 
   if (warp == 0) {
     if (lane == 0) {
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
       uint32_t c = 0;
       bool ok = true;
-      UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
-      for (; w.live() && ok; w.next()) {
-        const int rem = w.rem;
+      int4 e;
+      for (uint32_t i = 0; ok && queue.get(i, e, false, 0, abort_word, lim) && e.x >= 0; ++i) {
+        *taken = static_cast<int>(i) + 1;
+        const int rem = e.y, r0 = e.z, r1 = e.w;
         const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128;
         const int n0 = (rem % NT) * BN + static_cast<int>(rank) * (BN / 2);
-        for (int r = w.r0; r < w.r1; r += kChunk) {
+        for (int r = r0; r < r1; r += kChunk) {
           const uint32_t s = c % S, ph = (c / S) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_word, lim)) {
             ok = false;
@@ -436,7 +492,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           uint8_t* a_dst = ring + s * C::kStageBytes;
           uint8_t* b_dst = a_dst + C::kABytes;
-          const int live = w.r1 - r;
+          const int live = r1 - r;
           const bool zero = live < kChunk && (live & 15) != 0;  // last step holds next-group rows
           if (leader || zero) {
             // local completion: the even CTA's own half, or an odd-CTA chunk
@@ -446,7 +502,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d(a_dst, &map_x, bar, k0, r);
             tma_load_2d(a_dst + C::kBoxBytes, &map_x, bar, k0 + 64, r);
 #pragma unroll
-            for (int i = 0; i < BN / 128; ++i) tma_load_2d(b_dst + i * C::kBoxBytes, &map_dy, bar, n0 + 64 * i, r);
+            for (int i2 = 0; i2 < BN / 128; ++i2)
+              tma_load_2d(b_dst + i2 * C::kBoxBytes, &map_dy, bar, n0 + 64 * i2, r);
           } else {
             // completes on the even CTA's barrier; the bytes may land before
             // the expectation is registered (the count dips below zero
@@ -456,8 +513,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(a_dst, &map_x, bar, k0, r);
             tma_load_2d_pair(a_dst + C::kBoxBytes, &map_x, bar, k0 + 64, r);
 #pragma unroll
-            for (int i = 0; i < BN / 128; ++i)
-              tma_load_2d_pair(b_dst + i * C::kBoxBytes, &map_dy, bar, n0 + 64 * i, r);
+            for (int i2 = 0; i2 < BN / 128; ++i2)
+              tma_load_2d_pair(b_dst + i2 * C::kBoxBytes, &map_dy, bar, n0 + 64 * i2, r);
           }
           ++c;
         }
@@ -477,9 +534,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = make_idesc(1u /*bf16*/, true, true, 2 * kBM, BN);
     uint32_t c = 0, t = 0;
     bool ok = true;
-    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
-    for (; w.live() && ok; w.next()) {
-      const int r0 = w.r0, r1 = w.r1;
+    int4 e;
+    for (uint32_t i = 0; ok && queue.get(i, e, true, lane, abort_word, lim) && e.x >= 0; ++i) {
+      const int r0 = e.z, r1 = e.w;
       if (r1 <= r0) continue;  // empty group: the epilogues write zeros
       const uint32_t b = t & 1u, tph = (t >> 1) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&tempty[b], tph ^ 1u, abort_word, lim))) break;
@@ -530,10 +587,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);
     uint32_t c = 0, pp = 0;  // pp: parity of ploaded[s], one bit per slot
     bool ok = true;
-    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
-    for (; w.live() && ok; w.next()) {
-      for (int r = w.r0; r < w.r1; r += kChunk, ++c) {
-        const int live = w.r1 - r;
+    int4 e;
+    for (uint32_t i = 0; ok && queue.get(i, e, true, lane, abort_word, lim) && e.x >= 0; ++i) {
+      for (int r = e.z; r < e.w; r += kChunk, ++c) {
+        const int live = e.w - r;
         if (!(live < kChunk && (live & 15) != 0)) continue;
         const uint32_t s = c % S;
         if (!__all_sync(0xffffffffu, mbar_wait(&ploaded[s], (pp >> s) & 1u, abort_word, lim))) {
@@ -546,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_remote(full0 + s * 8u);
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp < kSchedWarp) {
     const int pw = warp - 2;
     const int h = pw >> 2;
     const int quad = warp & 3;
@@ -555,12 +612,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* box = staging + pw * 4096;
     uint8_t* brow = box + lane * 128;
     uint32_t t = 0;
-    UnitWalk w(offsets, args.order, KPNT, num_units, first, stride);
-    for (; w.live(); w.next()) {
-      const int g = w.g;
-      const int rem = w.rem;
+    int4 e;
+    for (uint32_t i = 0; queue.get(i, e, true, lane, abort_word, lim) && e.x >= 0; ++i) {
+      const int g = e.x;
+      const int rem = e.y;
       const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128, n0 = (rem % NT) * BN;
-      const int r0 = w.r0, r1 = w.r1;
+      const int r0 = e.z, r1 = e.w;
       const int y = g * args.K + k0 + quad * 32;
       uint32_t r[BN / 2];
       if (r1 <= r0) {
@@ -601,6 +658,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     if (lane == 0) bulk_wait_all();
+  } else if (leader && lane == 0) {
+    // ------------------------------------------------------------ scheduler
+    int* claimed = const_cast<int32_t*>(args.meta) + kWsClaimed;
+    const uint32_t odd_full = mapa_shared(smem_u32(qfull), 1);
+    const uint32_t odd_data = mapa_shared(smem_u32(qdata), 1);
+    uint32_t i = 0;
+    auto publish = [&](int4 v) -> bool {
+      const uint32_t slot = i % kQueue, ph = (i / kQueue) & 1u;
+      // no more than kClaimAhead entries beyond the producer (bounded wait)
+      if (*taken + kClaimAhead <= static_cast<int>(i)) {
+        const uint64_t t0 = global_timer_ns();
+        while (*taken + kClaimAhead <= static_cast<int>(i)) {
+          if (*abort_word) return false;
+          if (global_timer_ns() - t0 > lim) {
+            *abort_word = 1;
+            return false;
+          }
+          __nanosleep(64);
+        }
+      }
+      if (!mbar_wait(&qempty[slot], ph ^ 1u, abort_word, lim)) return false;
+      qdata[slot] = v;
+      fence_proxy_async_smem();  // the bulk copy reads the entry through the async proxy
+      mbar_arrive_expect_tx_remote(odd_full + slot * 8u, 16);
+      bulk_copy_s2cluster(odd_data + slot * 16u, &qdata[slot], 16, odd_full + slot * 8u);
+      mbar_arrive(&qfull[slot]);
+      ++i;
+      return true;
+    };
+    constexpr int kMaxBatch = 4;
+    bool ok = true;
+    int batch = 1, next_batch = 1;
+    int k = num_units > 0 ? atomicAdd(claimed, 1) : num_units;
+    while (ok && k < num_units) {
+      const int k0 = k, cnt = min(batch, num_units - k0);
+      k = atomicAdd(claimed, next_batch);  // the next claim is in flight while this one is resolved
+      batch = next_batch;
+      int g[kMaxBatch], r0[kMaxBatch], r1[kMaxBatch];
+#pragma unroll
+      for (int j = 0; j < kMaxBatch; ++j) g[j] = j < cnt ? __ldg(args.order + (k0 + j) / KPNT) : 0;
+#pragma unroll
+      for (int j = 0; j < kMaxBatch; ++j) {
+        r0[j] = j < cnt ? __ldg(offsets + g[j]) : 0;
+        r1[j] = j < cnt ? __ldg(offsets + g[j] + 1) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxBatch; ++j)
+        if (ok && j < cnt) ok = publish(make_int4(g[j], (k0 + j) % KPNT, r0[j], r1[j]));
+      // the units come largest first: claim more at once as they get small
+      const int chunks = (r1[cnt - 1] - r0[cnt - 1] + kChunk - 1) / kChunk;
+      next_batch = chunks >= 4 ? 1 : chunks >= 2 ? 2 : kMaxBatch;
+    }
+    if (ok) publish(make_int4(-1, 0, 0, 0));
   }
 
   // teardown: no CTA of the pair leaves while the other may still arrive on
@@ -612,7 +722,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tbase, C::kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
+  if (threadIdx.x == 0) {
+    int32_t* w = const_cast<int32_t*>(args.meta);
+    if (*abort_word) atomicOr(w + kWsStatus, kErrTimeout);
+    // every CTA has stopped claiming; the last one out resets the counters
+    __threadfence();
+    if (atomicAdd(w + kWsFinished, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(w + kWsClaimed, 0);
+      atomicExch(w + kWsFinished, 0);
+    }
+  }
 }
 
 template <int BN>
@@ -624,7 +743,7 @@ cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, con
   // as many pairs as can be resident at once (one CTA per SM)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * max_pairs, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int clusters = 0;
@@ -632,7 +751,7 @@ cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, con
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const int pairs = clusters < max_pairs ? clusters : max_pairs;
-  return launch_pdl(tgmm_pair_kernel<BN>, dim3(2 * pairs), dim3(kThreads), smem, stream, map_x, map_dy, map_dw,
+  return launch_pdl(tgmm_pair_kernel<BN>, dim3(2 * pairs), dim3(kPairThreads), smem, stream, map_x, map_dy, map_dw,
                     args);
 }
 

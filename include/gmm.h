@@ -81,13 +81,16 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32 word[1]  1 if this call's sizes were valid, else 0
  *   int32 word[2]  S = sum(group_sizes)        (M when invalid)
  *   int32 word[3]  T = number of row tiles      (0 when invalid)
+ *   int32 word[4], word[5]  set to 0: the work counters of tgmm_bf16 (units
+ *                  claimed, CTAs finished); each tgmm_bf16 launch claims its
+ *                  units from them and its last CTA sets them back to 0
  *   int32 word[8 + g], g = 0..G  exclusive prefix sums off_g (off_G = S)
  *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
  *                  every group cut into consecutive tiles of at most 128 rows,
  *                  groups in order, empty groups contributing none.
  *   int32 order[G] at byte offset gmm_tiles_offset(G) + 16 * (ceil(M/128) + G):
  *                  the group ids sorted by size, largest first (ties by id);
- *                  the tgmm kernels deal their work largest groups first.
+ *                  the tgmm kernels take their work largest groups first.
  * The grouped calls below run this step themselves unless they are given
  * group_sizes = NULL, in which case they read what this call (or an earlier
  * grouped call) left in the workspace.

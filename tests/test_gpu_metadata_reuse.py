@@ -49,3 +49,28 @@ def test_null_group_sizes_needs_a_workspace():
     ws = torch.zeros((2, 1, 1), dtype=torch.float32, device="cuda")
     with pytest.raises(ValueError):
         gmm.fp8_fwd(xq, xs, wq, ws, None)
+
+
+def test_tgmm_work_counters_return_to_zero():
+    """The CTA-pair tgmm claims its units from two workspace words (units
+    claimed, CTAs finished); each launch must leave them at zero, so that
+    back-to-back calls on one workspace, of different shapes, each see every
+    unit once and give the same bits as a call that ran its own metadata."""
+    rng = np.random.default_rng(11)
+    sizes = [700, 0, 3, 260, 129, 64, 1, 0, 900, 17]
+    G, M = len(sizes), sum(sizes) + 37
+    s = to_dev(np.array(sizes, np.int32))
+    shapes = [(512, 512), (256, 256), (512, 1024)]
+    data = []
+    for K, N in shapes:
+        x = to_dev_bf16(normal_bf16((M, K), 1.0, rng))
+        dy = to_dev_bf16(normal_bf16((M, N), 1.0, rng))
+        data.append((x, dy, gmm.tgmm(x, dy, s)))
+    work = gmm.group_metadata(s, M)
+    for _ in range(3):
+        for x, dy, ref in data:
+            got = gmm.tgmm(x, dy, None, workspace=work)
+            assert torch.equal(ref.view(torch.uint8), got.view(torch.uint8))
+    torch.cuda.synchronize()
+    assert work.status() == 0
+    assert work.buf[16:24].view(torch.int32).tolist() == [0, 0]  # words 4 and 5
