@@ -27,7 +27,16 @@ STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_
 EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "gmm_tiles_offset",
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
             "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
-            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout"]
+            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_tiled"]
+
+
+class TileConfig(ctypes.Structure):
+    """gmm_fp8_tile_config: bn (128 | 256), ctas (1 .. SMs), unit_order
+    (1 row-tile major, 2 column-block major); 0 keeps a field's default."""
+    _fields_ = [("bn", ctypes.c_int), ("ctas", ctypes.c_int), ("unit_order", ctypes.c_int)]
+
+    def astuple(self):
+        return (self.bn, self.ctas, self.unit_order)
 
 
 class GmmError(RuntimeError):
@@ -69,6 +78,9 @@ def load():
     lib.gmm_quantize_rhs.argtypes = [P, I, I64, I64, P, P, P]
     lib.gmm_fp8_fwd.restype = I
     lib.gmm_fp8_fwd.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
+    lib.gmm_fp8_fwd_tiled.restype = I
+    lib.gmm_fp8_fwd_tiled.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P,
+                                      ctypes.POINTER(TileConfig)]
     lib.gmm_bf16_fwd.restype = I
     lib.gmm_bf16_fwd.argtypes = [P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.tgmm_bf16.restype = I
@@ -136,6 +148,16 @@ def gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, wor
                 workspace_bytes, stream=None) -> int:
     return load().gmm_fp8_fwd(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
                               int(fuse_silu_mul), _p(out), _p(workspace), workspace_bytes, _s(stream))
+
+
+def gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace,
+                      workspace_bytes, stream=None, config=None) -> int:
+    """config: a TileConfig, a (bn, ctas, unit_order) tuple, or None (defaults)."""
+    if config is not None and not isinstance(config, TileConfig):
+        config = TileConfig(*config)
+    return load().gmm_fp8_fwd_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
+                                    int(fuse_silu_mul), _p(out), _p(workspace), workspace_bytes, _s(stream),
+                                    ctypes.byref(config) if config is not None else None)
 
 
 def gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
@@ -245,7 +267,8 @@ def quantize_rhs(w: torch.Tensor, stream=None):
     return wq, ws
 
 
-def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, stream=None):
+def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, stream=None, config=None):
+    """config: a tile configuration (see TileConfig), or None for the defaults."""
     M, K = xq.shape
     G, Nw, K2 = wq.shape
     assert K2 == K
@@ -253,8 +276,12 @@ def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, s
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
     ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
-    _check(gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes,
-                       stream), "gmm_fp8_fwd")
+    if config is None:
+        _check(gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes,
+                           stream), "gmm_fp8_fwd")
+    else:
+        _check(gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes,
+                                 stream, config), "gmm_fp8_fwd_tiled")
     return out
 
 

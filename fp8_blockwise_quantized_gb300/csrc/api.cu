@@ -210,10 +210,23 @@ gmm_status gmm_quantize_rhs(const void* w, int G, int64_t K, int64_t N, void* wq
 gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const float* ws, const int32_t* group_sizes,
                        int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
+  return gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, workspace_bytes,
+                           stream, nullptr);
+}
+
+gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
+                             const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul,
+                             void* out, void* workspace, size_t workspace_bytes, void* stream,
+                             const gmm_fp8_tile_config* config) {
   const int fuse = fuse_silu_mul ? 1 : 0;
   const int64_t Nw = fuse ? 2 * N : N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
+  const gmm_fp8_tile_config cfg = config ? *config : gmm_fp8_tile_config{0, 0, 0};
+  if (cfg.bn != 0 && cfg.bn != 128 && cfg.bn != 256) return GMM_ERR_UNSUPPORTED;
+  if (cfg.bn == 256 && N % 256 != 0) return GMM_ERR_UNSUPPORTED;
+  if (cfg.bn == 128 && fuse) return GMM_ERR_UNSUPPORTED;
+  if (cfg.ctas < 0 || cfg.unit_order < 0 || cfg.unit_order > 2) return GMM_ERR_UNSUPPORTED;
   if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !out)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(out) ||
@@ -222,11 +235,12 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
+  if (cfg.ctas > di.sms) return GMM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
 
-  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse);
+  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse, cfg.bn);
   CUtensorMap map_a, map_b, map_out;
   if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
   if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
@@ -242,9 +256,12 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
   a.K = static_cast<int>(K);
   a.N = static_cast<int>(N);
   a.fuse = fuse;
+  a.bn = geo.bn_mma;
+  a.col_major = cfg.unit_order == 2 ? 1 : 0;
   a.wait_limit_ns = wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
-  const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
+  const int ctas = cfg.ctas > 0 ? cfg.ctas : di.sms;
+  const int grid = static_cast<int>(max_units < ctas ? max_units : ctas);
   cudaError_t e = launch_gmm_fp8(map_a, map_b, map_out, a, grid, s);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 kernel launch");
 }

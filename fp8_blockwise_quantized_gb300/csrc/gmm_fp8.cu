@@ -62,22 +62,24 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kScaleSlots = 8;        // K blocks of scales in flight
 constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
 
-// This CTA's units u = blockIdx.x, + gridDim.x, ... (tile u / per_tile,
-// column block u % per_tile).  The next unit's tile is loaded one unit ahead,
-// so its global-memory latency overlaps the current unit instead of sitting
-// between two units on each role's path.
+// This CTA's units u = blockIdx.x, + gridDim.x, ...: tile u / per_tile and
+// column block u % per_tile (row-tile major), or tile u % num_tiles and
+// column block u / num_tiles (column-block major).  The next unit's tile is
+// loaded one unit ahead, so its global-memory latency overlaps the current
+// unit instead of sitting between two units on each role's path.
 struct TileWalk {
   const Tile* tiles;
   long long num, u;
-  int per;
+  int per, ntiles;
+  bool col_major;
   Tile cur, nxt;
-  __device__ TileWalk(const Tile* t, int per_tile, long long num_units)
-      : tiles(t), num(num_units), u(blockIdx.x), per(per_tile) {
+  __device__ TileWalk(const Tile* t, int per_tile, long long num_units, int num_tiles, bool column_major)
+      : tiles(t), num(num_units), u(blockIdx.x), per(per_tile), ntiles(num_tiles), col_major(column_major) {
     if (u < num) cur = load(u);
     prefetch();
   }
   __device__ Tile load(long long v) const {
-    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + v / per));
+    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + (col_major ? v % ntiles : v / per)));
     return Tile{q.x, q.y, q.z, q.w};
   }
   __device__ void prefetch() {
@@ -85,7 +87,7 @@ struct TileWalk {
     if (un < num) nxt = load(un);
   }
   __device__ bool live() const { return u < num; }
-  __device__ int col0(int cols) const { return static_cast<int>(u % per) * cols; }
+  __device__ int col0(int cols) const { return static_cast<int>(col_major ? u / ntiles : u % per) * cols; }
   __device__ void next() {
     u += gridDim.x;
     cur = nxt;
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = args.meta[kWsNumTiles];
   const int units_per_tile = args.N / C::kOutCols;
   const long long num_units = static_cast<long long>(num_tiles) * units_per_tile;
+  const bool col_major = args.col_major != 0;
   const int KB = args.K / 128;
   const int Nw = FUSE ? 2 * args.N : args.N;
   const uint64_t lim = args.wait_limit_ns;
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+      for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
         const Tile tl = w.cur;
         const int n0 = w.col0(C::kOutCols);
         const int brow = tl.g * Nw + n0;
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NBw = Nw / 128;
     uint32_t q = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int n0 = w.col0(C::kOutCols);
       // the (up to) two RHS column blocks this unit's accumulators use
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ store warp
     uint32_t ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int n0 = w.col0(C::kOutCols);
       if (!__all_sync(0xffffffffu, mbar_wait(staged, ue & 1u, abort_word, lim))) {
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t t = 0, ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int row = tl.row0 + quad * 32 + lane;
       const bool valid = row < tl.row1;
@@ -537,9 +540,9 @@ cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUt
 
 }  // namespace
 
-Fp8Geometry fp8_geometry(int N, int fuse) {
+Fp8Geometry fp8_geometry(int N, int fuse, int bn) {
   if (fuse) return {256, 128, 128};
-  if (N % 256 == 0) return {256, 256, 256};
+  if (bn == 256 || (bn == 0 && N % 256 == 0)) return {256, 256, 256};
   return {128, 128, 128};
 }
 
@@ -547,7 +550,8 @@ cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, c
                            const FwdArgs& args, int grid, cudaStream_t stream) {
   if (args.fuse && args.hq) return launch<256, true, true>(map_a, map_b, map_out, args, grid, stream);
   if (args.fuse) return launch<256, true, false>(map_a, map_b, map_out, args, grid, stream);
-  if (args.N % 256 == 0) return launch<256, false, false>(map_a, map_b, map_out, args, grid, stream);
+  if (args.bn == 256 || (args.bn == 0 && args.N % 256 == 0))
+    return launch<256, false, false>(map_a, map_b, map_out, args, grid, stream);
   return launch<128, false, false>(map_a, map_b, map_out, args, grid, stream);
 }
 

@@ -50,6 +50,8 @@ struct FwdArgs {
   float* hs;              // fused quantized output scales: fp32 [N/128][M]
   int M, K, N;            // N = output columns
   int fuse;               // 1: silu(gate) * up, W has 2N columns
+  int bn;                 // FP8: columns of W per unit (0: by N)
+  int col_major;          // FP8: units ordered column block major
   uint64_t wait_limit_ns;
 };
 
@@ -81,7 +83,7 @@ struct Fp8Geometry {
   int out_cols;    // output columns per work unit
   int b_box_rows;  // rows of the W tensor-map box
 };
-Fp8Geometry fp8_geometry(int N, int fuse);
+Fp8Geometry fp8_geometry(int N, int fuse, int bn = 0);
 Fp8Geometry bf16_geometry(int N, int fuse);
 int tgmm_bn(int N);
 

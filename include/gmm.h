@@ -142,6 +142,36 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
                        void* stream);
 
 /*
+ * Tile configuration of the FP8 forward, the space the autotuner searches
+ * ("GEMM Kernel 性能优化十问", Q8: tile sizes chosen by a search over measured
+ * candidates, each checked for accuracy).  Every configuration computes the
+ * same sums in the same order (each output element is one row tile's K loop
+ * of one unit); a field left 0 keeps the default.
+ *   bn          columns of W per work unit and MMA N: 128 or 256.  256 needs
+ *               N % 256 == 0 (default then); 128 is not available with
+ *               fuse_silu_mul = 1, whose units are 256 columns of W.
+ *   ctas        persistent CTAs, 1 .. the number of SMs (default: one per SM)
+ *   unit_order  1: row-tile major, the column blocks of a row tile run side
+ *               by side (default); 2: column-block major, the row tiles that
+ *               share a column block of an expert's weights run side by side
+ * A value outside these returns GMM_ERR_UNSUPPORTED before any launch.
+ */
+typedef struct {
+  int bn;
+  int ctas;
+  int unit_order;
+} gmm_fp8_tile_config;
+
+/*
+ * gmm_fp8_fwd with a tile configuration (config = NULL: the defaults, exactly
+ * gmm_fp8_fwd).  Same arguments, layouts, results and errors otherwise.
+ */
+gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
+                             const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
+                             int fuse_silu_mul, void* out, void* workspace, size_t workspace_bytes, void* stream,
+                             const gmm_fp8_tile_config* config);
+
+/*
  * FP8 forward of the gate/up layer with the next layer's quantization fused
  * into its epilogue: "MoE 优化的探索" §5.1 names the step between Linear-1 and
  * Linear-2 "SwiGLU / FP8 Cast"; here the wi kernel emits, besides (optionally)

@@ -84,6 +84,26 @@ def test_fp8_host_validation(lib, kw, code):
     assert _fp8(lib, **kw) == code
 
 
+def _tiled(lib, cfg, **kw):
+    import ctypes
+    from fp8_blockwise_quantized_gb300 import TileConfig
+    a = dict(xq=FAKE, xs=FAKE, wq=FAKE, ws=FAKE, gs=FAKE, G=4, M=512, K=256, N=256, fuse=0, out=FAKE,
+             work=FAKE, wbytes=1 << 20)
+    a.update(kw)
+    return lib.gmm_fp8_fwd_tiled(a["xq"], a["xs"], a["wq"], a["ws"], a["gs"], a["G"], a["M"], a["K"], a["N"],
+                                 a["fuse"], a["out"], a["work"], a["wbytes"], None, ctypes.byref(TileConfig(*cfg)))
+
+
+@pytest.mark.parametrize("cfg,kw,code", [
+    ((64, 0, 0), {}, 4), ((256, 0, 0), dict(N=384), 4), ((128, 0, 0), dict(fuse=1), 4),
+    ((0, -1, 0), {}, 4), ((0, 0, 3), {}, 4), ((0, 0, -1), {}, 4),
+    ((256, 0, 2), dict(K=100), 2), ((128, 0, 1), dict(wq=None), 1),
+])
+def test_tile_config_host_validation(lib, cfg, kw, code):
+    # rejected on the host, before any device call
+    assert _tiled(lib, cfg, **kw) == code
+
+
 def test_null_group_sizes_is_not_a_host_error(lib):
     # group_sizes = NULL reuses the workspace's metadata: shape errors are still
     # reported first, and a missing weight is still a null-pointer error

@@ -1,0 +1,85 @@
+"""The FP8 forward's tile configurations on the GPU: every configuration the
+autotuner may choose gives the default configuration's bits (the same sums in
+the same order), on ragged cases with empty groups, partial tiles and tail
+rows, plain and fused; the device-dependent configuration errors; and one
+short autotuner run whose winner passes the gate.  The default configuration
+itself is checked against the oracle in test_gpu_gmm.py."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_blockwise_quantized_gb300 as gmm
+from fp8_blockwise_quantized_gb300 import tune
+from fp8_blockwise_quantized_gb300.workloads import normal_bf16
+from tests.gpu_util import to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ([300, 0, 129, 1, 640], 1200, 512, 512),
+    ([77, 300, 1, 255, 256, 33], 1000, 256, 768),
+    ([0, 0, 0], 64, 256, 256),
+]
+
+
+def _problem(sizes, M, K, Nw, seed):
+    rng = np.random.default_rng(seed)
+    s = to_dev(np.array(sizes, np.int32))
+    x = to_dev_bf16(normal_bf16((M, K), 1.0, rng, outlier_p=0.01))
+    w = to_dev_bf16(normal_bf16((len(sizes), K, Nw), 1.0 / np.sqrt(K), rng))
+    xq, xs = gmm.quantize_lhs(x)
+    wq, ws = gmm.quantize_rhs(w)
+    return s, xq, xs, wq, ws
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("sizes,M,K,N", CASES)
+def test_every_config_gives_the_default_bits(sizes, M, K, N):
+    s, xq, xs, wq, ws = _problem(sizes, M, K, N, 5 + M)
+    ref = gmm.fp8_fwd(xq, xs, wq, ws, s)
+    sms = _sms()
+    bns = (128, 256) if N % 256 == 0 else (128,)
+    for bn in bns:
+        for ctas in (0, 1, 7, sms // 2, sms):
+            for order in (1, 2):
+                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(bn, ctas, order))
+                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (bn, ctas, order)
+
+
+def test_fused_configs_give_the_default_bits():
+    sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
+    s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 17)
+    ref = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True)
+    for ctas in (0, 3, _sms() // 2):
+        for order in (1, 2):
+            got = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(256, ctas, order))
+            assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (ctas, order)
+
+
+def test_config_errors_on_the_device():
+    s, xq, xs, wq, ws = _problem([100, 28], 128, 256, 384, 3)
+    for cfg in [(256, 0, 1), (0, _sms() + 1, 1), (64, 0, 1), (0, 0, 3)]:
+        with pytest.raises(gmm.GmmError) as e:
+            gmm.fp8_fwd(xq, xs, wq, ws, s, config=cfg)
+        assert e.value.status == 4, cfg
+    # the fused gate/up weight (2N = 512 columns) has 256-column units only
+    s, xq, xs, wq, ws = _problem([100, 28], 128, 256, 512, 4)
+    with pytest.raises(gmm.GmmError) as e:
+        gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(128, 0, 1))
+    assert e.value.status == 4
+
+
+def test_autotuner_winner_passes_the_gate():
+    sizes, M, K, N = [700, 0, 3, 260, 129, 64, 1, 900], 2100, 512, 512
+    s, xq, xs, wq, ws = _problem(sizes, M, K, N, 23)
+    r = tune.tune_fp8_fwd(xq, xs, wq, ws, s, generations=2, population=4, reps=2, seed=1)
+    sp = tune.space_for(N, False, _sms())
+    assert sp.contains(r.best) and r.default == tune.default_config(sp)
+    assert all(ok for _, _, _, ok in r.history)  # every configuration gives the default's bits
+    ref = gmm.fp8_fwd(xq, xs, wq, ws, s)
+    got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=r.best)
+    assert torch.equal(ref.view(torch.int16), got.view(torch.int16))
+    assert r.best_ms <= r.default_ms
