@@ -260,6 +260,7 @@ gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, co
   a.col_major = cfg.unit_order == 2 ? 1 : 0;
   a.wait_limit_ns = wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
+  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
   const int ctas = cfg.ctas > 0 ? cfg.ctas : di.sms;
   const int grid = static_cast<int>(max_units < ctas ? max_units : ctas);
   cudaError_t e = launch_gmm_fp8(map_a, map_b, map_out, a, grid, s);
@@ -310,6 +311,7 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   a.fuse = 1;
   a.wait_limit_ns = wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
+  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
   const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
   cudaError_t e = launch_gmm_fp8(map_a, map_b, map_h, a, grid, s);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 fused-quant kernel launch");

@@ -66,28 +66,28 @@ constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad
 // column block u % per_tile (row-tile major), or tile u % num_tiles and
 // column block u / num_tiles (column-block major).  The next unit's tile is
 // loaded one unit ahead, so its global-memory latency overlaps the current
-// unit instead of sitting between two units on each role's path.
+// unit instead of sitting between two units on each role's path.  The host
+// keeps the number of units below 2^31, so unit indices are 32-bit.
 struct TileWalk {
   const Tile* tiles;
-  long long num, u;
-  int per, ntiles;
+  uint32_t num, u, d;  // d: per_tile (row-tile major) or num_tiles (column-block major)
   bool col_major;
   Tile cur, nxt;
-  __device__ TileWalk(const Tile* t, int per_tile, long long num_units, int num_tiles, bool column_major)
-      : tiles(t), num(num_units), u(blockIdx.x), per(per_tile), ntiles(num_tiles), col_major(column_major) {
+  __device__ TileWalk(const Tile* t, uint32_t per_tile, uint32_t num_units, uint32_t num_tiles, bool column_major)
+      : tiles(t), num(num_units), u(blockIdx.x), d(column_major ? num_tiles : per_tile), col_major(column_major) {
     if (u < num) cur = load(u);
     prefetch();
   }
-  __device__ Tile load(long long v) const {
-    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + (col_major ? v % ntiles : v / per)));
+  __device__ Tile load(uint32_t v) const {
+    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + (col_major ? v % d : v / d)));
     return Tile{q.x, q.y, q.z, q.w};
   }
   __device__ void prefetch() {
-    const long long un = u + gridDim.x;
+    const uint32_t un = u + gridDim.x;
     if (un < num) nxt = load(un);
   }
   __device__ bool live() const { return u < num; }
-  __device__ int col0(int cols) const { return static_cast<int>(col_major ? u / ntiles : u % per) * cols; }
+  __device__ int col0(int cols) const { return static_cast<int>(col_major ? u / d : u % d) * cols; }
   __device__ void next() {
     u += gridDim.x;
     cur = nxt;
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int num_tiles = args.meta[kWsNumTiles];
   const int units_per_tile = args.N / C::kOutCols;
-  const long long num_units = static_cast<long long>(num_tiles) * units_per_tile;
+  const uint32_t num_units = static_cast<uint32_t>(num_tiles) * static_cast<uint32_t>(units_per_tile);
   const bool col_major = args.col_major != 0;
   const int KB = args.K / 128;
   const int Nw = FUSE ? 2 * args.N : args.N;
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc = make_idesc(0u /*e4m3*/, false, false, kBM, BN);
       uint32_t c = 0, t = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (uint32_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
           if (!mbar_wait(&full[s], ph, abort_word, lim)) {

@@ -146,6 +146,7 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   a.fuse = fuse;
   a.wait_limit_ns = kDefaultWaitLimitNs;
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
+  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
   const int grid = static_cast<int>(max_units < d.sms ? max_units : d.sms);
   return launch_gmm_fp8(map_a, map_b, map_out, a, grid, s) == cudaSuccess ? GMM_OK : GMM_ERR_CUDA;
 }
