@@ -135,6 +135,8 @@ gmm_status gmm_quantize_rhs(const void* w, int G, int64_t K, int64_t N, void* wq
  *   xq, xs    as written by gmm_quantize_lhs (M rows, K columns)
  *   wq, ws    as written by gmm_quantize_rhs (G, K, N or 2N)
  *   out       bf16 [M, N]; rows >= S are written as zeros
+ * GMM_ERR_SHAPE also when the work units, (ceil(M/128) + G) row tiles times
+ * N/256 (or N/128) column blocks, reach 2^31 (far beyond any real layer).
  */
 gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const float* ws,
                        const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
