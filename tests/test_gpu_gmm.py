@@ -72,6 +72,21 @@ def test_fp8_edges(sizes, M, K, N, fuse):
     assert np.all(got[S:] == 0), "rows past sum(group_sizes) must be zero"
 
 
+@pytest.mark.parametrize("scale", [40.0, 400.0])
+def test_fp8_fused_extreme_gates(scale):
+    """Gate values far into both tails of silu (|gate| up to ~1e3 and beyond
+    the -80 clamp of the kernel's silu), with an up factor of either sign."""
+    sizes, M, K, N = [200, 0, 185], 512, 256, 256
+    rng = np.random.default_rng(int(scale))
+    s = np.array(sizes, np.int32)
+    x = normal_bf16((M, K), scale, rng)
+    w = normal_bf16((len(sizes), K, 2 * N), 1.0 / np.sqrt(K), rng)
+    got = _run_fp8(s, x, w, True)
+    ref = _oracle_fp8(s, x, w, True)
+    assert np.max(np.abs(ref)) > 100.0 and np.min(ref) < 0.0
+    assert_close(got, ref, FP8_ATOL, FP8_RTOL, "fused fp8 fwd, extreme gates")
+
+
 @pytest.mark.parametrize("fuse", [False, True])
 @pytest.mark.parametrize("sizes,M,K,N", EDGE)
 def test_bf16_edges(sizes, M, K, N, fuse):
