@@ -681,7 +681,7 @@ def main():
                     choices=["fp8_wi", "fp8_wi_quant", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
                     help="run one kernel at the production shape (for ncu) and exit")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes per launch of the dominant kernel, if captured for this build")
+                    help="ncu dram bytes per launch of the dominant kernel, if captured on the current kernel source")
     args = ap.parse_args()
     if args.warmup < 3 and not args.profile_case:
         ap.error("--warmup must be >= 3")
