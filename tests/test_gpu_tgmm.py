@@ -52,3 +52,27 @@ def test_tgmm_dev_shape_full():
     torch.cuda.synchronize()
     ref = oracle.tgmm_bf16(c.x, c.dy, c.group_sizes)
     assert_close(bf16_to_np64(dw), ref, BF16_ATOL, BF16_RTOL, "tgmm dev")
+
+
+def test_tgmm_many_small_groups():
+    """4096 groups (the largest G), most of them empty or a few rows long, a
+    few large: thousands of units, most with one partial chunk, which the
+    CTA pairs claim several at a time; every dW[g] against the oracle and the
+    empty groups' tiles zero."""
+    rng = np.random.default_rng(4096)
+    G, K, N = 4096, 256, 128  # the CTA-pair kernel with 128-column units
+    sizes = np.where(rng.random(G) < 0.5, 0, rng.integers(1, 9, G)).astype(np.int32)
+    sizes[[7, 1000, 4095]] = [700, 130, 64]
+    M = int(sizes.sum()) + 5
+    x = normal_bf16((M, K), 1.0, rng)
+    dy = normal_bf16((M, N), 1.0, rng)
+    dw = poison_bf16(torch.empty((G, K, N), dtype=torch.bfloat16, device="cuda"))
+    work = gmm.Workspace(G, M)
+    gmm.tgmm(to_dev_bf16(x), to_dev_bf16(dy), to_dev(sizes), dw=dw, workspace=work)
+    torch.cuda.synchronize()
+    assert work.status() == 0
+    assert work.buf[16:24].view(torch.int32).tolist() == [0, 0]  # work counters back at zero
+    got = bf16_to_np64(dw)
+    ref = oracle.tgmm_bf16(x, dy, sizes)
+    assert_close(got, ref, BF16_ATOL, BF16_RTOL, "tgmm, 4096 groups")
+    assert np.all(got[sizes == 0] == 0)
