@@ -376,6 +376,7 @@ def run_gpu(args):
 
     # ---------------- bf16 forward baseline, timed beside the step (not in it)
     bf = {}
+    dgrad = None
     if not args.no_bf16_baseline:
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         tb = []
@@ -398,6 +399,29 @@ def run_gpu(args):
               "wo_TFLOP/s": round(flops["gmm_fp8_wo"] / (wo_ms * 1e-3) / 1e12, 1),
               "fp8_over_bf16_gmm_only": round((wi_ms + wo_ms) / fp8_ms, 3),
               "fp8_over_bf16_with_quantize": round((wi_ms + wo_ms) / (fp8_ms + q_ms), 3)}
+
+        # the layer's bf16 data gradients beside the step (not in it):
+        # dH = dY . W_wo[g]^T and dX = d(gate|up) . W_wi[g]^T
+        tdg = []
+        for i in range(max(3, args.steps)):
+            flush.zero_()
+            ev[0].record(stream)
+            chk(gmm.gmm_bf16_dgrad(dy, w_wo, sizes, G, M, N, K, h, work.buf, work.nbytes, stream), "dgrad dH")
+            ev[1].record(stream)
+            chk(gmm.gmm_bf16_dgrad(dh, w_wi, sizes, G, M, K, 2 * N, y, work.buf, work.nbytes, stream), "dgrad dX")
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                tdg.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        dh_ms = float(np.mean([a for a, _ in tdg]))
+        dx_ms = float(np.mean([b for _, b in tdg]))
+        bf_peak = peaks["bf16"]
+        dgrad = {"dH_ms": round(dh_ms, 4), "dX_ms": round(dx_ms, 4),
+                 "dH_TFLOP/s": round(flops["gmm_fp8_wo"] / (dh_ms * 1e-3) / 1e12, 1),
+                 "dX_TFLOP/s": round(flops["gmm_fp8_wi"] / (dx_ms * 1e-3) / 1e12, 1),
+                 "frac_bf16_peak": round((flops["gmm_fp8_wo"] + flops["gmm_fp8_wi"]) /
+                                         ((dh_ms + dx_ms) * 1e-3) / 1e12 / bf_peak, 3),
+                 "note": "bf16 dgrad of the layer (dY . W_wo^T, d(gate|up) . W_wi^T), timed beside the step"}
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -505,7 +529,7 @@ def run_gpu(args):
         "roofline": roof, "kernels": kern,
         "kernels_note": f"per-kernel times from a second pass of {n_split} steps with an event between every "
                         "call (the timed steps carry boundary events only)",
-        "bf16_fwd_baseline": bf or None, "e2e": e2e,
+        "bf16_fwd_baseline": bf or None, "bf16_dgrad": dgrad, "e2e": e2e,
         "cpu_baseline": cpu, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
