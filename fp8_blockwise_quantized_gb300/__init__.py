@@ -1,8 +1,9 @@
 """GB300 (sm_103a) MoE grouped matmul with blockwise FP8 quantization.
 
 The computation lives in the CUDA library ``libgmm_gb300.so`` (C ABI in
-``include/gmm.h``); this package holds its Python binding, its build script
-and the seeded synthetic workloads.
+``include/gmm.h``); this package holds its Python binding, its build script,
+the seeded synthetic workloads and the FP8 tile autotuner (``tune``:
+``python -m fp8_blockwise_quantized_gb300.tune`` tunes the production layer).
 """
 from .binding import (EXPORTED, GmmError, LIB_PATH, STATUS_NAMES, Workspace, bf16_fwd, dgrad, fp8_fwd,
                       gmm_bf16_dgrad, gmm_selftest_wait_timeout, gmm_fp8_fwd_swiglu_quant, fp8_fwd_swiglu_quant,
