@@ -27,6 +27,10 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 
 }  // namespace
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // LHS, 1x128 blocks.  X is row-major [M, K] with K % 128 == 0; block (m, kb)
 // occupies bytes [256 (m KB + kb), + 256) of X.  A half-warp (16 lanes x 16
 // bytes) handles one block; a warp handles the blocks kb of eight consecutive
@@ -48,6 +52,17 @@ __global__ void __launch_bounds__(256) quantize_lhs_kernel(const uint4* __restri
 
   const long long nslots = ((M + 7) / 8) * 8LL * KB;
   for (long long base = warp_id * kLhsBlocksPerWarp; base < nslots; base += nwarps * kLhsBlocksPerWarp) {
+    {
+      // the warp's next step: its 16 lines (8 rows x 256 bytes) into L2 now,
+      // so that the loads of that step find them there (one step ahead is
+      // what helps; two steps ahead evicts lines before they are used)
+      const long long nb = base + nwarps * kLhsBlocksPerWarp;
+      if (lane < 16 && nb < nslots) {
+        const long long g2 = nb >> 3;
+        const long long m2 = (g2 / KB) * 8 + (lane >> 1), k2 = g2 - (g2 / KB) * KB;
+        if (m2 < M) prefetch_l2(x + (m2 * KB + k2) * 16 + (lane & 1) * 8);
+      }
+    }
     uint4 v[kPerHalf];
     const long long grp = base >> 3;
     const long long mg = grp / KB, kbg = grp - mg * KB;
