@@ -11,8 +11,9 @@
 // How (sm_103a).  The quantization block is decoupled from the pipeline: the
 // MMA never stops at a block boundary, only its accumulator buffer changes.
 //   warp 0      TMA producer: per K block one 128x128 B Xq tile and one
-//               BNx128 B Wq tile (K-major, 128-byte swizzle) into a 4-stage
-//               shared-memory ring, completion counted on an mbarrier.
+//               BNx128 B Wq tile (K-major, 128-byte swizzle) into a shared-
+//               memory ring (3 stages of 48 KB with BN = 256, 4 of 32 KB with
+//               BN = 128), completion counted on an mbarrier.
 //   warp 1      allocates TMEM and issues tcgen05.mma (kind::f8f6f4, M=128,
 //               N=BN, K=32, four per K block) into one of two TMEM partial
 //               buffers; tcgen05.commit frees the ring slot and publishes the

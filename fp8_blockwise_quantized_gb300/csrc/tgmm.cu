@@ -19,8 +19,10 @@
 //              TMA tensor store per box; zero tile for an empty group.  The
 //              small staging area leaves room for a 4-slot load ring.
 // TMEM holds two accumulators, so one tile's epilogue overlaps the next
-// tile's MMAs.  Units are ordered group-major so the tiles of one group (which
-// share its x and dy rows) run together.
+// tile's MMAs.  Units are numbered group-major, largest groups first, so the
+// tiles of one group (which share its x and dy rows) run together; this
+// single-CTA kernel (K not a multiple of 256) deals them in snake rounds, the
+// CTA-pair kernel below claims them from a counter.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
