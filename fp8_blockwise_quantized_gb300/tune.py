@@ -166,11 +166,11 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, generations: i
 
 
 def main(argv=None):
-    """Tune the production MoE layer's two FP8 launches on this GPU and print
+    """Tune the production MoE layer's two FP8 forwards on this GPU and print
     every measured configuration: the fused wi (G=256, M=65536, K=2048, W with
-    2 x 512 columns, writing h and its FP8 cast) and wo (K=512, N=2048 on the
-    FP8 cast of h).  Inputs are the seeded synthetic production workload
-    (Zipf(1.1) top-8 routing, X N(0,1) with 1% x50 outliers, W N(0, 1/K))."""
+    2 x 512 columns, writing h) and wo (K=512, N=2048 on the FP8 cast of h).
+    Inputs are the seeded synthetic production workload (Zipf(1.1) top-8
+    routing, X N(0,1) with 1% x50 outliers, W N(0, 1/K))."""
     import argparse
     import json
     import math
