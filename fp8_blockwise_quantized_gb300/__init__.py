@@ -7,14 +7,16 @@ the seeded synthetic workloads and the FP8 tile autotuner (``tune``:
 """
 from .binding import (EXPORTED, GmmError, LIB_PATH, STATUS_NAMES, Workspace, bf16_fwd, dgrad, fp8_fwd,
                       gmm_bf16_dgrad, gmm_selftest_wait_timeout, gmm_fp8_fwd_swiglu_quant, fp8_fwd_swiglu_quant,
-                      gmm_bf16_fwd, gmm_fp8_fwd, gmm_fp8_fwd_noalloc, gmm_fp8_fwd_tiled, gmm_get_device_status,
+                      gmm_bf16_fwd, gmm_fp8_fwd, gmm_fp8_fwd_noalloc, gmm_fp8_fwd_tiled,
+                      gmm_fp8_fwd_swiglu_quant_tiled, gmm_get_device_status,
                       gmm_group_metadata, TileConfig,
                       gmm_quantize_lhs, gmm_quantize_rhs, gmm_tiles_offset, gmm_workspace_bytes,
                       group_metadata, load, quantize_lhs, quantize_rhs, tgmm, tgmm_bf16)
 
 __all__ = ["EXPORTED", "GmmError", "LIB_PATH", "STATUS_NAMES", "Workspace", "bf16_fwd", "dgrad", "fp8_fwd",
            "gmm_bf16_dgrad", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_swiglu_quant", "fp8_fwd_swiglu_quant",
-           "gmm_bf16_fwd", "gmm_fp8_fwd", "gmm_fp8_fwd_noalloc", "gmm_fp8_fwd_tiled", "gmm_get_device_status",
+           "gmm_bf16_fwd", "gmm_fp8_fwd", "gmm_fp8_fwd_noalloc", "gmm_fp8_fwd_tiled",
+           "gmm_fp8_fwd_swiglu_quant_tiled", "gmm_get_device_status",
            "gmm_group_metadata", "TileConfig",
            "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_tiles_offset", "gmm_workspace_bytes",
            "group_metadata", "load", "quantize_lhs", "quantize_rhs", "tgmm", "tgmm_bf16"]

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_
 EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "gmm_tiles_offset",
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
             "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
-            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_tiled"]
+            "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_tiled",
+            "gmm_fp8_fwd_swiglu_quant_tiled"]
 
 
 class TileConfig(ctypes.Structure):
@@ -87,6 +88,9 @@ def load():
     lib.tgmm_bf16.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
     lib.gmm_fp8_fwd_swiglu_quant.restype = I
     lib.gmm_fp8_fwd_swiglu_quant.argtypes = [P, P, P, P, P, I, I64, I64, I64, P, P, P, P, SZ, P]
+    lib.gmm_fp8_fwd_swiglu_quant_tiled.restype = I
+    lib.gmm_fp8_fwd_swiglu_quant_tiled.argtypes = [P, P, P, P, P, I, I64, I64, I64, P, P, P, P, SZ, P,
+                                                   ctypes.POINTER(TileConfig)]
     lib.gmm_bf16_dgrad.restype = I
     lib.gmm_bf16_dgrad.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
     lib.gmm_get_device_status.restype = I
@@ -164,6 +168,16 @@ def gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs,
                              workspace_bytes, stream=None) -> int:
     return load().gmm_fp8_fwd_swiglu_quant(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N, _p(h),
                                            _p(hq), _p(hs), _p(workspace), workspace_bytes, _s(stream))
+
+
+def gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
+                                   workspace_bytes, stream=None, config=None) -> int:
+    """config: a TileConfig, a (bn, ctas, unit_order) tuple, or None (defaults)."""
+    if config is not None and not isinstance(config, TileConfig):
+        config = TileConfig(*config)
+    return load().gmm_fp8_fwd_swiglu_quant_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
+                                                 _p(h), _p(hq), _p(hs), _p(workspace), workspace_bytes, _s(stream),
+                                                 ctypes.byref(config) if config is not None else None)
 
 
 def gmm_bf16_fwd(x, w, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, workspace_bytes,
@@ -285,18 +299,28 @@ def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, s
     return out
 
 
-def fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, with_h=True, workspace=None, stream=None):
-    """Fused wi: returns (h or None, hq [M, N] e4m3 codes, hs [N/128, M])."""
+def fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, with_h=True, workspace=None, stream=None, config=None,
+                         out=None):
+    """Fused wi: returns (h or None, hq [M, N] e4m3 codes, hs [N/128, M]).
+    config: a tile configuration (see TileConfig), or None for the defaults;
+    out: an (h, hq, hs) triple to write into instead of new tensors."""
     M, K = xq.shape
     G, Nw, K2 = wq.shape
     assert K2 == K
     N = Nw // 2
-    h = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if with_h else None
-    hq = torch.empty((M, N), dtype=torch.uint8, device=xq.device)
-    hs = torch.empty((N // 128, M), dtype=torch.float32, device=xq.device)
+    if out is not None:
+        h, hq, hs = out
+    else:
+        h = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if with_h else None
+        hq = torch.empty((M, N), dtype=torch.uint8, device=xq.device)
+        hs = torch.empty((N // 128, M), dtype=torch.float32, device=xq.device)
     ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
-    _check(gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, ws_.buf, ws_.nbytes,
-                                    stream), "gmm_fp8_fwd_swiglu_quant")
+    if config is None:
+        _check(gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, ws_.buf, ws_.nbytes,
+                                        stream), "gmm_fp8_fwd_swiglu_quant")
+    else:
+        _check(gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, ws_.buf,
+                                              ws_.nbytes, stream, config), "gmm_fp8_fwd_swiglu_quant_tiled")
     return h, hq, hs
 
 

@@ -270,9 +270,20 @@ gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, co
 gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq, const float* ws,
                                     const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
                                     void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream) {
+  return gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
+                                        workspace_bytes, stream, nullptr);
+}
+
+gmm_status gmm_fp8_fwd_swiglu_quant_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
+                                          const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
+                                          void* h, void* hq, float* hs, void* workspace, size_t workspace_bytes,
+                                          void* stream, const gmm_fp8_tile_config* config) {
   const int64_t Nw = 2 * N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
+  const gmm_fp8_tile_config cfg = config ? *config : gmm_fp8_tile_config{0, 0, 0};
+  if ((cfg.bn != 0 && cfg.bn != 256) || cfg.ctas < 0 || cfg.unit_order < 0 || cfg.unit_order > 2)
+    return GMM_ERR_UNSUPPORTED;
   if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !hq || !hs)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(h) || !aligned16(hq) ||
@@ -281,6 +292,7 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
+  if (cfg.ctas > di.sms) return GMM_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
@@ -309,10 +321,13 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
   a.K = static_cast<int>(K);
   a.N = static_cast<int>(N);
   a.fuse = 1;
+  a.bn = geo.bn_mma;
+  a.col_major = cfg.unit_order == 2 ? 1 : 0;
   a.wait_limit_ns = wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
   if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
-  const int grid = static_cast<int>(max_units < di.sms ? max_units : di.sms);
+  const int ctas = cfg.ctas > 0 ? cfg.ctas : di.sms;
+  const int grid = static_cast<int>(max_units < ctas ? max_units : ctas);
   cudaError_t e = launch_gmm_fp8(map_a, map_b, map_h, a, grid, s);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 fused-quant kernel launch");
 }

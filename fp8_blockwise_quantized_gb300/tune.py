@@ -120,15 +120,19 @@ def evolve(evaluate, space: Space, generations: int = 4, population: int = 6, ke
     return Result(best, best_ms, d, seen[d][0], history)
 
 
-def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, generations: int = 4, population: int = 6,
-                 keep: int = 2, seed: int = 0, reps: int = 5, atol: float | None = None,
+def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = False, generations: int = 4,
+                 population: int = 6, keep: int = 2, seed: int = 0, reps: int = 5, atol: float | None = None,
                  rtol: float | None = None, stream=None) -> Result:
     """Search gmm_fp8_tile_config for this problem on the current device.
 
-    The inputs are those of ``binding.fp8_fwd``. Each candidate runs ``reps``
-    times after one untimed run; its time is the median. With atol/rtol left
-    None the gate is bit-exact against the default's output; given, it is
+    The inputs are those of ``binding.fp8_fwd``. ``quant`` tunes the fused
+    forward that also writes h's FP8 cast (``fp8_fwd_swiglu_quant``, the wi
+    launch of the MoE layer); its gate compares h, the codes and the scales
+    bit for bit. Each candidate runs ``reps`` times after one untimed run,
+    and its time is the median. With atol/rtol left None, the gate for the
+    plain forward is bit-exact against the default's output; given, it is
     torch.allclose with them."""
+    fuse = fuse or quant
     dev = xq.device
     M, K = xq.shape
     G, Nw, _ = wq.shape
@@ -136,23 +140,41 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, generations: i
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     space = space_for(N, fuse, sms)
     work = binding.group_metadata(group_sizes, M)
-    ref = binding.fp8_fwd(xq, xs, wq, ws, None, fuse=fuse, workspace=work, stream=stream)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream(dev) if stream is None else stream
 
-    def evaluate(c):
-        out = torch.empty_like(ref)
-        binding.fp8_fwd(xq, xs, wq, ws, None, fuse=fuse, out=out, workspace=work, stream=st, config=c)
-        if atol is None and rtol is None:
-            ok = torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    def run(c, outs):
+        if quant:
+            binding.fp8_fwd_swiglu_quant(xq, xs, wq, ws, None, workspace=work, stream=st, config=c, out=outs)
         else:
-            ok = torch.allclose(out.float(), ref.float(), atol=atol or 0.0, rtol=rtol or 0.0)
+            binding.fp8_fwd(xq, xs, wq, ws, None, fuse=fuse, out=outs[0], workspace=work, stream=st, config=c)
+
+    def alloc():
+        if quant:
+            return (torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                    torch.empty((M, N), dtype=torch.uint8, device=dev),
+                    torch.empty((N // 128, M), dtype=torch.float32, device=dev))
+        return (torch.empty((M, N), dtype=torch.bfloat16, device=dev),)
+
+    ref = alloc()
+    run(None, ref)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def same_bits(a, b):
+        return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+    def evaluate(c):
+        outs = alloc()
+        run(c, outs)
+        if quant or (atol is None and rtol is None):
+            ok = all(same_bits(a, b) for a, b in zip(outs, ref))
+        else:
+            ok = torch.allclose(outs[0].float(), ref[0].float(), atol=atol or 0.0, rtol=rtol or 0.0)
         times = []
         for _ in range(reps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
-            binding.fp8_fwd(xq, xs, wq, ws, None, fuse=fuse, out=out, workspace=work, stream=st, config=c)
+            run(c, outs)
             e1.record(st)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
@@ -166,9 +188,10 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, generations: i
 
 
 def main(argv=None):
-    """Tune the production MoE layer's two FP8 forwards on this GPU and print
+    """Tune the production MoE layer's two FP8 launches on this GPU and print
     every measured configuration: the fused wi (G=256, M=65536, K=2048, W with
-    2 x 512 columns, writing h) and wo (K=512, N=2048 on the FP8 cast of h).
+    2 x 512 columns, writing h and its FP8 cast) and wo (K=512, N=2048 on the
+    FP8 cast of h).
     Inputs are the seeded synthetic production workload (Zipf(1.1) top-8
     routing, X N(0,1) with 1% x50 outliers, W N(0, 1/K))."""
     import argparse
@@ -198,8 +221,8 @@ def main(argv=None):
     wq_wo, ws_wo = binding.quantize_rhs(w_wo)
     _, hq, hs = binding.fp8_fwd_swiglu_quant(xq, xs, wq_wi, ws_wi, sizes, with_h=False)
     out = {}
-    for name, a, fuse in [("wi_fused", (xq, xs, wq_wi, ws_wi), True), ("wo", (hq, hs, wq_wo, ws_wo), False)]:
-        r = tune_fp8_fwd(*a, sizes, fuse=fuse, generations=args.generations, population=args.population,
+    for name, a, quant in [("wi_fused_cast", (xq, xs, wq_wi, ws_wi), True), ("wo", (hq, hs, wq_wo, ws_wo), False)]:
+        r = tune_fp8_fwd(*a, sizes, quant=quant, generations=args.generations, population=args.population,
                          reps=args.reps, seed=args.seed)
         out[name] = {"best": list(r.best), "best_us": round(r.best_ms * 1e3, 1), "default": list(r.default),
                      "default_us": round(r.default_ms * 1e3, 1),

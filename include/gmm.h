@@ -189,6 +189,16 @@ gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void*
                                     void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gmm_fp8_fwd_swiglu_quant with a tile configuration (gmm_fp8_tile_config
+ * above; bn must be 0 or 256, the fused units being 256 columns of W;
+ * config = NULL: exactly gmm_fp8_fwd_swiglu_quant).
+ */
+gmm_status gmm_fp8_fwd_swiglu_quant_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
+                                          const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
+                                          void* h, void* hq, float* hs, void* workspace, size_t workspace_bytes,
+                                          void* stream, const gmm_fp8_tile_config* config);
+
+/*
  * a7 — bf16 GMM forward, unquantized (the BF16 baseline of "GEMM Kernel
  * 性能优化十问", Q7/Q10 step 4): out[m,n] = bf16(sum_k x[m,k] * w[g,k,n]),
  * fp32 accumulation; fuse_silu_mul as for gmm_fp8_fwd.

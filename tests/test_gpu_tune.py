@@ -83,3 +83,26 @@ def test_autotuner_winner_passes_the_gate():
     got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=r.best)
     assert torch.equal(ref.view(torch.int16), got.view(torch.int16))
     assert r.best_ms <= r.default_ms
+
+
+def test_fused_cast_configs_give_the_default_bits():
+    """The wi launch that also writes h's FP8 cast: h, the e4m3 codes and the
+    scales of every configuration equal the default's."""
+    sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
+    s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 29)
+    ref = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s)
+    for ctas in (0, 5, _sms() // 2):
+        for order in (1, 2):
+            got = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(256, ctas, order))
+            for a, b in zip(ref, got):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (ctas, order)
+    with pytest.raises(gmm.GmmError) as e:
+        gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(128, 0, 1))
+    assert e.value.status == 4
+
+
+def test_autotuner_on_the_fused_cast_launch():
+    sizes, M, K, N = [700, 0, 3, 260, 129, 64, 1, 900], 2100, 512, 256
+    s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 31)
+    r = tune.tune_fp8_fwd(xq, xs, wq, ws, s, quant=True, generations=2, population=3, reps=2, seed=2)
+    assert r.best[0] == 256 and all(ok for _, _, _, ok in r.history)
