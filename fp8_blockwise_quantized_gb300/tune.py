@@ -139,8 +139,8 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
     N = Nw // 2 if fuse else Nw
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     space = space_for(N, fuse, sms)
-    work = binding.group_metadata(group_sizes, M)
     st = torch.cuda.current_stream(dev) if stream is None else stream
+    work = binding.group_metadata(group_sizes, M, stream=st)
 
     def run(c, outs):
         if quant:
@@ -157,6 +157,7 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
 
     ref = alloc()
     run(None, ref)
+    st.synchronize()  # the comparisons below run on torch's current stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def same_bits(a, b):
@@ -165,6 +166,7 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
     def evaluate(c):
         outs = alloc()
         run(c, outs)
+        st.synchronize()
         if quant or (atol is None and rtol is None):
             ok = all(same_bits(a, b) for a, b in zip(outs, ref))
         else:
@@ -172,6 +174,7 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
         times = []
         for _ in range(reps):
             flush.zero_()
+            torch.cuda.current_stream(dev).synchronize()  # the flush, before the timed launch
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
             run(c, outs)
@@ -181,7 +184,7 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
         times.sort()
         return times[len(times) // 2], bool(ok)
 
-    status = work.status()
+    status = work.status(st)
     if status != binding.GMM_OK:
         raise RuntimeError(f"group metadata: {binding.STATUS_NAMES.get(status, status)}")
     return evolve(evaluate, space, generations, population, keep, seed)
