@@ -8,8 +8,12 @@ inv = 0 if scale == 0 else 1/scale, q = e4m3(x * inv).
 The pins do not retype that formula: they check closed forms (a block whose
 absmax is 448 has scale exactly 1; power-of-two rescaling), the quantization
 error bound of e4m3, block locality (an element only touches its own block's
-scale and codes), and the scale against numpy's IEEE fp32 division.
+scale and codes), the scale against numpy's IEEE fp32 division, and hand-
+derived points (tests/golden/quant_reciprocal_points.txt) at which multiplying
+by the fp32-rounded reciprocal and dividing by the scale give different codes.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -138,3 +142,67 @@ def test_rhs_matches_lhs_on_a_single_block_row():
 def test_lhs_rejects_bad_k(bad):
     with pytest.raises(Exception):
         oracle.quantize_lhs(np.zeros(bad, np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# multiply by the rounded reciprocal, not divide ("实现差距：GMM Kernel（V1 vs
+# V2）", §3.3 takes 1/scale once and multiplies every element by it).  The
+# points in tests/golden/quant_reciprocal_points.txt were derived by hand so
+# that the two readings give different codes; the oracle must give the
+# multiply reading's code, and each point must really separate the readings.
+# ---------------------------------------------------------------------------
+
+RECIP_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "quant_reciprocal_points.txt")
+
+
+def _recip_points():
+    pts = []
+    for line in open(RECIP_GOLDEN):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        a, x, mul_code, div_code = line.split()
+        ev = lambda e: float(eval(e, {"__builtins__": {}}))
+        pts.append((ev(a), ev(x), int(mul_code, 16), int(div_code, 16)))
+    return pts
+
+
+def _bits(v):
+    b = f32_to_bf16_bits(np.array([v], np.float32))[0]
+    assert float(bf16_bits_to_f32(np.array([b], np.uint16))[0]) == v, f"{v} is not a bf16 value"
+    return b
+
+
+def test_reciprocal_points_lhs():
+    pts = _recip_points()
+    assert len(pts) >= 12 and all(m != d for _, _, m, d in pts)
+    x = np.zeros((len(pts), 256), np.uint16)
+    for i, (a, v, _, _) in enumerate(pts):
+        # the absmax and the probed element in block 1 of row i, at positions
+        # that move with i; block 0 holds the same pair mirrored
+        x[i, 128 + (i * 7) % 128] = _bits(a)
+        x[i, 128 + (i * 7 + 61) % 128] = _bits(v)
+        x[i, (i * 11 + 3) % 128] = _bits(-a)
+        x[i, (i * 11 + 90) % 128] = _bits(v)
+    xq, xs = oracle.quantize_lhs(x)
+    for i, (a, v, mul, div) in enumerate(pts):
+        assert xs[i, 1] == np.float32(a) / np.float32(448.0) and xs[i, 0] == xs[i, 1]
+        assert xq[i, 128 + (i * 7 + 61) % 128] == mul, (a, v, hex(xq[i, 128 + (i * 7 + 61) % 128]), hex(mul))
+        assert xq[i, (i * 11 + 90) % 128] == mul
+        assert xq[i, 128 + (i * 7) % 128] == 0x7E and xq[i, (i * 11 + 3) % 128] == 0xFE
+        assert xq[i, 128 + (i * 7 + 61) % 128] != div
+
+
+def test_reciprocal_points_rhs():
+    pts = _recip_points()
+    G = len(pts)
+    w = np.zeros((G, 128, 256), np.uint16)
+    for g, (a, v, _, _) in enumerate(pts):
+        w[g, (g * 5) % 128, 128 + (g * 3) % 128] = _bits(a)
+        w[g, (g * 5 + 40) % 128, 128 + (g * 3 + 77) % 128] = _bits(v)
+    wq, ws = oracle.quantize_rhs(w)
+    for g, (a, v, mul, div) in enumerate(pts):
+        assert ws[g, 0, 1] == np.float32(a) / np.float32(448.0) and ws[g, 0, 0] == 0.0
+        got = wq[g, (g * 5 + 40) % 128, 128 + (g * 3 + 77) % 128]
+        assert got == mul and got != div, (a, v, hex(got))
+        assert wq[g, (g * 5) % 128, 128 + (g * 3) % 128] == 0x7E
