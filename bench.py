@@ -631,6 +631,51 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# the oracle on the four small configurations, whole (not sampled): all host
+# cores, and one core in a child process (OpenMP reads its thread count once)
+# ---------------------------------------------------------------------------
+
+ORACLE_CONFIGS = ["tiny_fp8", "wi_dev_fp8", "wo_dev_fp8", "tgmm_dev_bf16"]
+
+
+def _oracle_config_pass(name: str):
+    """One whole pass of the oracle on a configuration (weights quantized
+    outside the timing, as on the GPU); returns (seconds, GFLOP)."""
+    import oracle
+    from fp8_blockwise_quantized_gb300.workloads import make_case
+    oracle.build()
+    c = make_case(name)
+    if name == "tgmm_dev_bf16":
+        t0 = time.perf_counter()
+        oracle.tgmm_bf16(c.x, c.dy, c.group_sizes)
+        dt = time.perf_counter() - t0
+        return dt, 2.0 * c.M * c.K * c.N / 1e9
+    wq, ws = oracle.quantize_rhs(c.w)
+    t0 = time.perf_counter()
+    xq, xs = oracle.quantize_lhs(c.x)
+    oracle.round_to_bf16(oracle.gmm_fp8(xq, xs, wq, ws, c.group_sizes))
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * c.M * c.K * c.N / 1e9
+
+
+def run_oracle_configs():
+    import oracle
+    oracle.build()
+    rows = []
+    for name in ORACLE_CONFIGS:
+        dt_all, gf = _oracle_config_pass(name)
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-config-one", name],
+                             env=env, capture_output=True, text=True, check=True)
+        one = json.loads(out.stdout.strip().splitlines()[-1])
+        rows.append({"config": name, "gflop": round(gf, 3), "all_cores_s": round(dt_all, 3),
+                     "cores": oracle.num_threads(), "one_core_s": round(one["seconds"], 3),
+                     "all_cores_gflops": round(gf / dt_all, 3), "one_core_gflops": round(gf / one["seconds"], 3)})
+    print(json.dumps({"oracle_configs": rows, "what": "quantize X + FP8 GMM (weights quantized beforehand) "
+                                                      "or bf16 tgmm, whole configuration, one pass"}))
+
+
+# ---------------------------------------------------------------------------
 # single-kernel mode for profilers: production shapes, only what one kernel needs
 # ---------------------------------------------------------------------------
 
@@ -704,9 +749,19 @@ def main():
     ap.add_argument("--profile-case", default=None,
                     choices=["fp8_wi", "fp8_wi_quant", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
                     help="run one kernel at the production shape (for ncu) and exit")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="time the CPU oracle on the four small configurations (all cores and one core) and exit")
+    ap.add_argument("--oracle-config-one", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per launch of the dominant kernel, if captured on the current kernel source")
     args = ap.parse_args()
+    if args.oracle_config_one:
+        dt, gf = _oracle_config_pass(args.oracle_config_one)
+        print(json.dumps({"seconds": dt, "gflop": gf}))
+        return
+    if args.oracle_configs:
+        run_oracle_configs()
+        return
     if args.warmup < 3 and not args.profile_case:
         ap.error("--warmup must be >= 3")
     if args.profile_case:

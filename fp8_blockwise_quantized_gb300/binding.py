@@ -20,6 +20,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgmm_gb300.so")
 
 GMM_OK = 0
+GMM_ERR_GROUP_SIZES = 6
+GMM_ERR_TIMEOUT = 7
 STATUS_NAMES = {0: "GMM_OK", 1: "GMM_ERR_NULL", 2: "GMM_ERR_SHAPE", 3: "GMM_ERR_ALIGN",
                 4: "GMM_ERR_UNSUPPORTED", 5: "GMM_ERR_CUDA", 6: "GMM_ERR_GROUP_SIZES",
                 7: "GMM_ERR_TIMEOUT", 8: "GMM_ERR_WORKSPACE"}

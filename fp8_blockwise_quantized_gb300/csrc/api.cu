@@ -12,18 +12,44 @@
 
 #include "gmm.h"
 #include "common.cuh"
+#include "host.cuh"
 #include "kernels.cuh"
 
 using namespace gmm;
 
 namespace {
-
 thread_local char g_last_error[256] = "no error";
+}  // namespace
 
-gmm_status cuda_fail(cudaError_t e, const char* what) {
+namespace gmm {
+
+gmm_status host_cuda_fail(cudaError_t e, const char* what) {
   std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
   return GMM_ERR_CUDA;
 }
+
+gmm_status host_fail(gmm_status status, const char* what) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s", what);
+  return status;
+}
+
+uint64_t host_wait_limit_ns() {
+  static uint64_t v = []() -> uint64_t {
+    const char* s = std::getenv("GMM_WAIT_LIMIT_MS");
+    if (s && *s) {
+      long long ms = std::atoll(s);
+      if (ms > 0) return static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    return static_cast<uint64_t>(kDefaultWaitLimitNs);
+  }();
+  return v;
+}
+
+}  // namespace gmm
+
+namespace {
+
+gmm_status cuda_fail(cudaError_t e, const char* what) { return host_cuda_fail(e, what); }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -74,17 +100,7 @@ gmm_status device_info(DeviceInfo* out) {
   return GMM_OK;
 }
 
-uint64_t wait_limit_ns() {
-  static uint64_t v = []() -> uint64_t {
-    const char* s = std::getenv("GMM_WAIT_LIMIT_MS");
-    if (s && *s) {
-      long long ms = std::atoll(s);
-      if (ms > 0) return static_cast<uint64_t>(ms) * 1000000ull;
-    }
-    return static_cast<uint64_t>(kDefaultWaitLimitNs);
-  }();
-  return v;
-}
+uint64_t wait_limit_ns() { return host_wait_limit_ns(); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -18,6 +18,7 @@
 
 #include "gmm.h"
 #include "common.cuh"
+#include "host.cuh"
 #include "kernels.cuh"
 
 using namespace gmm;
@@ -50,28 +51,29 @@ gmm_status noalloc_setup(NoAllocDevice* out, EncodeTiledFn* encode) {
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) return e != cudaSuccess ? GMM_ERR_CUDA : GMM_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return host_cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return host_fail(GMM_ERR_UNSUPPORTED, "device ordinal beyond 63");
   std::lock_guard<std::mutex> lk(mu);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return GMM_ERR_CUDA;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return host_cuda_fail(e, "looking up cuTensorMapEncodeTiled");
+    if (q != cudaDriverEntryPointSuccess) return host_fail(GMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     fn = reinterpret_cast<EncodeTiledFn>(p);
   }
   NoAllocDevice& d = cache[dev];
   if (!d.ready) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return GMM_ERR_CUDA;
-    if (major != 10 || minor != 3) return GMM_ERR_UNSUPPORTED;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return host_cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) return host_fail(GMM_ERR_UNSUPPORTED, "the current device is not sm_103");
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr) return GMM_ERR_CUDA;
+    if (e != cudaSuccess) return host_cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+    if (ptr == nullptr) return host_fail(GMM_ERR_CUDA, "cudaGetSymbolAddress returned NULL");
     d.scratch = ptr;
     d.sms = sms;
     d.ready = true;
@@ -91,7 +93,7 @@ gmm_status encode(EncodeTiledFn fn, CUtensorMap* map, const void* base, uint64_t
   CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
+  return r == CUDA_SUCCESS ? GMM_OK : host_fail(GMM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 }
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -121,12 +123,13 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   // The scratch keeps whatever the previous call left; only the sticky error
   // word must start at zero (every other field is rewritten below).
   int32_t* meta = static_cast<int32_t*>(d.scratch);
-  if (cudaMemsetAsync(meta + kWsStatus, 0, sizeof(int32_t), s) != cudaSuccess) return GMM_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(meta + kWsStatus, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return host_cuda_fail(e, "clearing the static scratch's error word");
   Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(d.scratch) + tiles_offset_bytes(G));
   int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(d.scratch) + order_offset_bytes(G, M));
-  if (launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, s, group_sizes, G, static_cast<int>(M), meta,
-                 tiles, order) != cudaSuccess)
-    return GMM_ERR_CUDA;
+  e = launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, s, group_sizes, G, static_cast<int>(M), meta, tiles,
+                 order);
+  if (e != cudaSuccess) return host_cuda_fail(e, "group_metadata_kernel launch");
   if (M == 0) return GMM_OK;
 
   const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse);
@@ -144,9 +147,10 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   a.K = static_cast<int>(K);
   a.N = static_cast<int>(N);
   a.fuse = fuse;
-  a.wait_limit_ns = kDefaultWaitLimitNs;
+  a.wait_limit_ns = host_wait_limit_ns();
   const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
   if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
   const int grid = static_cast<int>(max_units < d.sms ? max_units : d.sms);
-  return launch_gmm_fp8(map_a, map_b, map_out, a, grid, s) == cudaSuccess ? GMM_OK : GMM_ERR_CUDA;
+  e = launch_gmm_fp8(map_a, map_b, map_out, a, grid, s);
+  return e == cudaSuccess ? GMM_OK : host_cuda_fail(e, "gmm_fp8 kernel launch");
 }

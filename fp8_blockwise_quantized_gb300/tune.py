@@ -120,6 +120,16 @@ def evolve(evaluate, space: Space, generations: int = 4, population: int = 6, ke
     return Result(best, best_ms, d, seen[d][0], history)
 
 
+def status_passes(status: int, where: str = "") -> bool:
+    """Whether a candidate's runs left the workspace's sticky error word
+    clear.  A candidate whose launch hit a bounded-wait timeout stopped early,
+    so its time would look short: it fails the gate.  Invalid group sizes are
+    the caller's error, not the candidate's: they raise."""
+    if status == binding.GMM_ERR_GROUP_SIZES:
+        raise RuntimeError(f"{where}: {binding.STATUS_NAMES[status]}")
+    return status == binding.GMM_OK
+
+
 def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = False, generations: int = 4,
                  population: int = 6, keep: int = 2, seed: int = 0, reps: int = 5, atol: float | None = None,
                  rtol: float | None = None, stream=None) -> Result:
@@ -158,19 +168,26 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
     ref = alloc()
     run(None, ref)
     st.synchronize()  # the comparisons below run on torch's current stream
+    status = work.status(st)
+    if status != binding.GMM_OK:
+        raise RuntimeError(f"default configuration: {binding.STATUS_NAMES.get(status, status)}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def same_bits(a, b):
         return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
 
+    def device_ok(where):
+        return status_passes(work.status(st), where)
+
     def evaluate(c):
         outs = alloc()
         run(c, outs)
         st.synchronize()
+        ok = device_ok(f"config {c}")
         if quant or (atol is None and rtol is None):
-            ok = all(same_bits(a, b) for a, b in zip(outs, ref))
+            ok = ok and all(same_bits(a, b) for a, b in zip(outs, ref))
         else:
-            ok = torch.allclose(outs[0].float(), ref[0].float(), atol=atol or 0.0, rtol=rtol or 0.0)
+            ok = ok and torch.allclose(outs[0].float(), ref[0].float(), atol=atol or 0.0, rtol=rtol or 0.0)
         times = []
         for _ in range(reps):
             flush.zero_()
@@ -181,12 +198,10 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
             e1.record(st)
             e1.synchronize()
             times.append(e0.elapsed_time(e1))
+        ok = device_ok(f"config {c}, timed runs") and ok
         times.sort()
         return times[len(times) // 2], bool(ok)
 
-    status = work.status(st)
-    if status != binding.GMM_OK:
-        raise RuntimeError(f"group metadata: {binding.STATUS_NAMES.get(status, status)}")
     return evolve(evaluate, space, generations, population, keep, seed)
 
 

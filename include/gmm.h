@@ -24,6 +24,11 @@
  *     a kernel's bounded wait running out set a sticky error word inside the
  *     workspace; the kernels then stop early and the outputs are undefined.
  *     gmm_get_device_status() reads and clears that word.  No kernel traps.
+ *     Every wait is limited to 2 s of GPU time by default; the environment
+ *     variable GMM_WAIT_LIMIT_MS (a positive number of milliseconds, read
+ *     once per process) changes the limit for every entry point.
+ *   - On GMM_ERR_CUDA (and the host-side errors that name a cause),
+ *     gmm_last_cuda_error() gives the calling thread's last message.
  *   - Row-major layouts; bf16 = IEEE bfloat16; e4m3 = OCP FP8 E4M3 (max 448).
  *   - K and N are multiples of 128 (the quantization block); 1 <= G <= 4096;
  *     0 <= M < 2^31.  M = 0, or every group empty, is valid.
@@ -259,6 +264,8 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
  *     the next; each call rewrites all it reads.  Calls that overlap on the
  *     GPU (different streams without ordering between them) race on it and
  *     must not be issued.
+ *   - Bounded waits, GMM_WAIT_LIMIT_MS and gmm_last_cuda_error() behave as
+ *     for every other entry point.
  *   - Device-detected errors (invalid group_sizes, a wait that ran out) are
  *     not reported by this entry point: the array's error word is cleared at
  *     the start of every call and cannot be read through this ABI; on such an

@@ -49,3 +49,36 @@ def poison_bf16(t: torch.Tensor) -> torch.Tensor:
     """Fill with NaN so that any element a kernel forgets to write shows up."""
     t.view(torch.int16).fill_(0x7FC0)
     return t
+
+
+GUARD_BYTES = 4096
+_GUARD_BEFORE, _GUARD_AFTER = 0xA5, 0x5A
+
+
+class Guarded:
+    """An output tensor with canary bands in front of it and behind it, in
+    the same device allocation (the out-of-bounds check that stands in for a
+    memory sanitizer): a kernel that writes past either end of its output
+    changes a band, and check() then fails.  The tensor starts 4096 bytes
+    into the allocation, so it keeps the 16-byte alignment the library needs;
+    poison=True fills a bf16 tensor with NaN (unwritten elements show up)."""
+
+    def __init__(self, shape, dtype, poison=True, device="cuda"):
+        itemsize = torch.empty((), dtype=dtype).element_size()
+        n = int(np.prod(shape)) * itemsize
+        self.n = n
+        self.raw = torch.empty(2 * GUARD_BYTES + n, dtype=torch.uint8, device=device)
+        self.raw[:GUARD_BYTES].fill_(_GUARD_BEFORE)
+        self.raw[GUARD_BYTES + n:].fill_(_GUARD_AFTER)
+        self.t = self.raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+        if poison and dtype == torch.bfloat16:
+            poison_bf16(self.t)
+        elif poison:
+            self.t.view(torch.uint8).fill_(0xEE)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        before = self.raw[:GUARD_BYTES]
+        after = self.raw[GUARD_BYTES + self.n:]
+        assert torch.all(before == _GUARD_BEFORE), f"{what}: a write landed in the band before the output"
+        assert torch.all(after == _GUARD_AFTER), f"{what}: a write landed in the band after the output"

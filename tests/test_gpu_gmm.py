@@ -8,7 +8,7 @@ import torch
 import oracle
 import fp8_blockwise_quantized_gb300 as gmm
 from fp8_blockwise_quantized_gb300.workloads import make_case, normal_bf16
-from tests.gpu_util import (BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, assert_close, bf16_to_np64,
+from tests.gpu_util import (BF16_ATOL, BF16_RTOL, FP8_ATOL, FP8_RTOL, Guarded, assert_close, bf16_to_np64,
                             poison_bf16, to_dev, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -45,12 +45,13 @@ def _run_fp8(s, x, w, fuse):
     N = Nw // 2 if fuse else Nw
     xq, xs = gmm.quantize_lhs(to_dev_bf16(x))
     wq, ws = gmm.quantize_rhs(to_dev_bf16(w))
-    out = poison_bf16(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+    out = Guarded((M, N), torch.bfloat16)
     work = gmm.Workspace(G, M)
-    gmm.fp8_fwd(xq, xs, wq, ws, to_dev(s), fuse=fuse, out=out, workspace=work)
+    gmm.fp8_fwd(xq, xs, wq, ws, to_dev(s), fuse=fuse, out=out.t, workspace=work)
     torch.cuda.synchronize()
     assert work.status() == 0
-    return bf16_to_np64(out)
+    out.check("fp8 fwd output")
+    return bf16_to_np64(out.t)
 
 
 def _oracle_fp8(s, x, w, fuse):
@@ -92,13 +93,14 @@ def test_fp8_fused_extreme_gates(scale):
 def test_bf16_edges(sizes, M, K, N, fuse):
     s, x, w = _inputs(sizes, M, K, 2 * N if fuse else N, M + K + N + 1)
     G = len(sizes)
-    out = poison_bf16(torch.empty((M, N), dtype=torch.bfloat16, device="cuda"))
+    out = Guarded((M, N), torch.bfloat16)
     work = gmm.Workspace(G, M)
-    gmm.bf16_fwd(to_dev_bf16(x), to_dev_bf16(w), to_dev(s), fuse=fuse, out=out, workspace=work)
+    gmm.bf16_fwd(to_dev_bf16(x), to_dev_bf16(w), to_dev(s), fuse=fuse, out=out.t, workspace=work)
     torch.cuda.synchronize()
     assert work.status() == 0
+    out.check("bf16 fwd output")
     ref = oracle.gmm_bf16(x, w, s, fuse=fuse)
-    assert_close(bf16_to_np64(out), ref, BF16_ATOL, BF16_RTOL, "bf16 fwd")
+    assert_close(bf16_to_np64(out.t), ref, BF16_ATOL, BF16_RTOL, "bf16 fwd")
 
 
 def test_fp8_tiny_config():

@@ -6,7 +6,8 @@ import torch
 import oracle
 import fp8_blockwise_quantized_gb300 as gmm
 from fp8_blockwise_quantized_gb300.workloads import make_case, normal_bf16
-from tests.gpu_util import BF16_ATOL, BF16_RTOL, assert_close, bf16_to_np64, poison_bf16, to_dev, to_dev_bf16
+from tests.gpu_util import (BF16_ATOL, BF16_RTOL, Guarded, assert_close, bf16_to_np64, poison_bf16, to_dev,
+                            to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,15 +32,16 @@ def test_tgmm_edges(sizes, M, K, N):
     G = len(sizes)
     x = normal_bf16((M, K), 1.0, rng)
     dy = normal_bf16((M, N), 1.0, rng)
-    dw = poison_bf16(torch.empty((G, K, N), dtype=torch.bfloat16, device="cuda"))
+    dwg = Guarded((G, K, N), torch.bfloat16)
     work = gmm.Workspace(G, M)
     xt = to_dev_bf16(x) if M else torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
     dyt = to_dev_bf16(dy) if M else torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
-    gmm.tgmm(xt, dyt, to_dev(s), dw=dw, workspace=work)
+    gmm.tgmm(xt, dyt, to_dev(s), dw=dwg.t, workspace=work)
     torch.cuda.synchronize()
     assert work.status() == 0
+    dwg.check("tgmm dW")
     ref = oracle.tgmm_bf16(x, dy, s)
-    got = bf16_to_np64(dw)
+    got = bf16_to_np64(dwg.t)
     assert_close(got, ref, BF16_ATOL, BF16_RTOL, "tgmm")
     for g in range(G):
         if sizes[g] == 0:
@@ -66,11 +68,13 @@ def test_tgmm_many_small_groups():
     M = int(sizes.sum()) + 5
     x = normal_bf16((M, K), 1.0, rng)
     dy = normal_bf16((M, N), 1.0, rng)
-    dw = poison_bf16(torch.empty((G, K, N), dtype=torch.bfloat16, device="cuda"))
+    dwg = Guarded((G, K, N), torch.bfloat16)
+    dw = dwg.t
     work = gmm.Workspace(G, M)
     gmm.tgmm(to_dev_bf16(x), to_dev_bf16(dy), to_dev(sizes), dw=dw, workspace=work)
     torch.cuda.synchronize()
     assert work.status() == 0
+    dwg.check("tgmm dW, 4096 groups")
     assert work.buf[16:24].view(torch.int32).tolist() == [0, 0]  # work counters back at zero
     got = bf16_to_np64(dw)
     ref = oracle.tgmm_bf16(x, dy, sizes)

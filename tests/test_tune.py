@@ -75,3 +75,13 @@ def test_evolve_is_deterministic_for_a_seed():
     a = tune.evolve(lambda c: (_cost(c), True), sp, generations=3, population=5, seed=9)
     b = tune.evolve(lambda c: (_cost(c), True), sp, generations=3, population=5, seed=9)
     assert a.history == b.history
+
+
+def test_a_timed_out_candidate_fails_the_gate():
+    from fp8_blockwise_quantized_gb300 import binding
+    assert tune.status_passes(binding.GMM_OK)
+    # a bounded wait ran out: the launch stopped early and its time is no
+    # measurement, so the candidate fails (and never becomes a parent)
+    assert not tune.status_passes(binding.GMM_ERR_TIMEOUT)
+    with pytest.raises(RuntimeError):
+        tune.status_passes(binding.GMM_ERR_GROUP_SIZES, "config (256, 152, 1)")
