@@ -35,11 +35,14 @@ EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "
 
 class TileConfig(ctypes.Structure):
     """gmm_fp8_tile_config: bn (128 | 256), ctas (1 .. SMs), unit_order
-    (1 row-tile major, 2 column-block major); 0 keeps a field's default."""
-    _fields_ = [("bn", ctypes.c_int), ("ctas", ctypes.c_int), ("unit_order", ctypes.c_int)]
+    (1 row-tile major, 2 column-block major), cta_group (1 one CTA per
+    128-row tile, 2 CTA pairs on 256-row tiles); 0 keeps a field's default.
+    A shorter tuple leaves the remaining fields 0."""
+    _fields_ = [("bn", ctypes.c_int), ("ctas", ctypes.c_int), ("unit_order", ctypes.c_int),
+                ("cta_group", ctypes.c_int)]
 
     def astuple(self):
-        return (self.bn, self.ctas, self.unit_order)
+        return (self.bn, self.ctas, self.unit_order, self.cta_group)
 
 
 class GmmError(RuntimeError):
@@ -158,7 +161,7 @@ def gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, wor
 
 def gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace,
                       workspace_bytes, stream=None, config=None) -> int:
-    """config: a TileConfig, a (bn, ctas, unit_order) tuple, or None (defaults)."""
+    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group]) tuple, or None (defaults)."""
     if config is not None and not isinstance(config, TileConfig):
         config = TileConfig(*config)
     return load().gmm_fp8_fwd_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
@@ -174,7 +177,7 @@ def gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs,
 
 def gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
                                    workspace_bytes, stream=None, config=None) -> int:
-    """config: a TileConfig, a (bn, ctas, unit_order) tuple, or None (defaults)."""
+    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group]) tuple, or None (defaults)."""
     if config is not None and not isinstance(config, TileConfig):
         config = TileConfig(*config)
     return load().gmm_fp8_fwd_swiglu_quant_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
@@ -243,10 +246,19 @@ class Workspace:
         off = gmm_tiles_offset(self.G)
         return self.buf[off:off + 16 * n].view(torch.int32).view(n, 4)[:, :3]
 
+    def _order_offset(self) -> int:
+        return gmm_tiles_offset(self.G) + 16 * ((self.M + 127) // 128 + self.G)
+
     def order(self) -> list[int]:
         """The group ids sorted by size, largest first (ties by id)."""
-        off = gmm_tiles_offset(self.G) + 16 * ((self.M + 127) // 128 + self.G)
+        off = self._order_offset()
         return self.buf[off:off + 4 * self.G].view(torch.int32).tolist()
+
+    def pair_tiles(self) -> torch.Tensor:
+        """The 256-row tiles {g, row0, row1} (the CTA-pair FP8 kernel's)."""
+        n = self.buf[24:28].view(torch.int32).item()
+        off = self._order_offset() + 16 * ((self.G + 3) // 4)
+        return self.buf[off:off + 16 * n].view(torch.int32).view(n, 4)[:, :3]
 
 
 def _ws(ws, G, M, device):

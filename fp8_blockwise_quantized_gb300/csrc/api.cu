@@ -135,11 +135,7 @@ gmm_status check_grouped(int G, int64_t M, int64_t K, int64_t N, int64_t Nw) {
 }
 
 gmm_status launch_metadata(const int32_t* sizes, int G, int64_t M, void* workspace, cudaStream_t st) {
-  int32_t* ws = static_cast<int32_t*>(workspace);
-  Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(workspace) + tiles_offset_bytes(G));
-  int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + order_offset_bytes(G, M));
-  cudaError_t e = launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, st, sizes, G, static_cast<int>(M), ws,
-                             tiles, order);
+  cudaError_t e = launch_group_metadata(sizes, G, static_cast<int>(M), workspace, st);
   return e == cudaSuccess ? GMM_OK : cuda_fail(e, "group_metadata_kernel launch");
 }
 
@@ -151,6 +147,88 @@ gmm_status check_workspace(const void* workspace, size_t bytes, int G, int64_t M
 }
 
 }  // namespace
+
+namespace gmm {
+
+int host_fp8_default_cta_group(int64_t, int, int, int) {
+  // one CTA per tile: on the production shapes the CTA-pair kernel measured
+  // 316 / 171 us against 191 / 124 us (wi / wo); its N = 128 pair MMAs issue
+  // far below their math rate
+  return 1;
+}
+
+gmm_status host_fp8_config(int64_t N, int fuse, const gmm_fp8_tile_config* in, int sms, gmm_fp8_tile_config* out) {
+  gmm_fp8_tile_config c = in ? *in : gmm_fp8_tile_config{0, 0, 0, 0};
+  if (c.cta_group == 0) c.cta_group = host_fp8_default_cta_group(N, fuse, c.bn, c.ctas);
+  if (c.cta_group != 1 && c.cta_group != 2) return GMM_ERR_UNSUPPORTED;
+  if (c.bn != 0 && c.bn != 128 && c.bn != 256) return GMM_ERR_UNSUPPORTED;
+  if (c.ctas < 0 || (sms > 0 && c.ctas > sms) || c.unit_order < 0 || c.unit_order > 2) return GMM_ERR_UNSUPPORTED;
+  if (c.cta_group == 2) {
+    // units of 256 weight columns (two MMA halves of 128): 128 gate + 128 up
+    // columns when fused, else 256 output columns
+    if (c.bn == 128 || (!fuse && N % 256 != 0)) return GMM_ERR_UNSUPPORTED;
+    if (c.ctas % 2 != 0) return GMM_ERR_UNSUPPORTED;
+    c.bn = 256;
+  } else {
+    if (c.bn == 256 && N % 256 != 0) return GMM_ERR_UNSUPPORTED;
+    if (c.bn == 128 && fuse) return GMM_ERR_UNSUPPORTED;
+    if (c.bn == 0) c.bn = (fuse || N % 256 == 0) ? 256 : 128;
+  }
+  if (c.ctas == 0) c.ctas = c.cta_group == 2 ? sms - sms % 2 : sms;
+  if (c.unit_order == 0) c.unit_order = 1;
+  *out = c;
+  return GMM_OK;
+}
+
+gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, const float* ws, int G, int64_t M,
+                           int64_t K, int64_t N, int fuse, void* out, void* hq, float* hs, void* workspace,
+                           const gmm_fp8_tile_config& cfg, cudaStream_t s) {
+  const bool pair = cfg.cta_group == 2;
+  const int64_t Nw = fuse ? 2 * N : N;
+  // MMA N per unit, output columns per unit, rows of the weight tensor-map box
+  const Fp8Geometry geo = pair ? Fp8Geometry{128, fuse ? 128 : 256, 64} : fp8_geometry(static_cast<int>(N), fuse, cfg.bn);
+  CUtensorMap map_a, map_b, map_out;
+  gmm_status st;
+  if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
+  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
+    return st;
+  // the bf16 output is written through its own tensor map; the fused cast
+  // without h stores only hq and hs and never reads map_out
+  if (out) {
+    if ((st = encode_2d(&map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, N, M, 64, 32)) != GMM_OK) return st;
+  } else {
+    map_out = map_a;
+  }
+  FwdArgs a{};
+  a.xs = xs;
+  a.ws = ws;
+  a.meta = static_cast<const int32_t*>(workspace);
+  a.tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + tiles_offset_bytes(G));
+  a.pair_tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + pair_tiles_offset_bytes(G, M));
+  a.out = static_cast<uint16_t*>(out);
+  a.hq = static_cast<uint8_t*>(hq);
+  a.hs = hs;
+  a.M = static_cast<int>(M);
+  a.K = static_cast<int>(K);
+  a.N = static_cast<int>(N);
+  a.fuse = fuse;
+  a.bn = geo.bn_mma;
+  a.col_major = cfg.unit_order == 2 ? 1 : 0;
+  a.wait_limit_ns = host_wait_limit_ns();
+  const long long tiles = pair ? pair_tiles_capacity(G, M) : tiles_capacity(G, M);
+  const long long max_units = tiles * (N / geo.out_cols);
+  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernels' unit indices are 32-bit
+  cudaError_t e;
+  if (pair) {
+    const long long pairs = cfg.ctas / 2;
+    e = launch_gmm_fp8_pair(map_a, map_b, map_out, a, static_cast<int>(max_units < pairs ? max_units : pairs), s);
+  } else {
+    e = launch_gmm_fp8(map_a, map_b, map_out, a, static_cast<int>(max_units < cfg.ctas ? max_units : cfg.ctas), s);
+  }
+  return e == cudaSuccess ? GMM_OK : host_cuda_fail(e, "gmm_fp8 kernel launch");
+}
+
+}  // namespace gmm
 
 extern "C" {
 
@@ -238,49 +316,21 @@ gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, co
   const int64_t Nw = fuse ? 2 * N : N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
-  const gmm_fp8_tile_config cfg = config ? *config : gmm_fp8_tile_config{0, 0, 0};
-  if (cfg.bn != 0 && cfg.bn != 128 && cfg.bn != 256) return GMM_ERR_UNSUPPORTED;
-  if (cfg.bn == 256 && N % 256 != 0) return GMM_ERR_UNSUPPORTED;
-  if (cfg.bn == 128 && fuse) return GMM_ERR_UNSUPPORTED;
-  if (cfg.ctas < 0 || cfg.unit_order < 0 || cfg.unit_order > 2) return GMM_ERR_UNSUPPORTED;
   if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !out)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(out) ||
       !aligned16(group_sizes))
     return GMM_ERR_ALIGN;
+  gmm_fp8_tile_config cfg;
+  if ((st = host_fp8_config(N, fuse, config, 0, &cfg)) != GMM_OK) return st;  // the device-independent rules
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
-  if (cfg.ctas > di.sms) return GMM_ERR_UNSUPPORTED;
+  if ((st = host_fp8_config(N, fuse, config, di.sms, &cfg)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
-
-  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse, cfg.bn);
-  CUtensorMap map_a, map_b, map_out;
-  if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
-  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
-    return st;
-  if ((st = encode_2d(&map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, N, M, 64, 32)) != GMM_OK) return st;
-  FwdArgs a{};
-  a.xs = xs;
-  a.ws = ws;
-  a.meta = static_cast<const int32_t*>(workspace);
-  a.tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + tiles_offset_bytes(G));
-  a.out = static_cast<uint16_t*>(out);
-  a.M = static_cast<int>(M);
-  a.K = static_cast<int>(K);
-  a.N = static_cast<int>(N);
-  a.fuse = fuse;
-  a.bn = geo.bn_mma;
-  a.col_major = cfg.unit_order == 2 ? 1 : 0;
-  a.wait_limit_ns = wait_limit_ns();
-  const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
-  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
-  const int ctas = cfg.ctas > 0 ? cfg.ctas : di.sms;
-  const int grid = static_cast<int>(max_units < ctas ? max_units : ctas);
-  cudaError_t e = launch_gmm_fp8(map_a, map_b, map_out, a, grid, s);
-  return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 kernel launch");
+  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, nullptr, nullptr, workspace, cfg, s);
 }
 
 gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq, const float* ws,
@@ -297,55 +347,21 @@ gmm_status gmm_fp8_fwd_swiglu_quant_tiled(const void* xq, const float* xs, const
   const int64_t Nw = 2 * N;
   gmm_status st = check_grouped(G, M, K, N, Nw);
   if (st != GMM_OK) return st;
-  const gmm_fp8_tile_config cfg = config ? *config : gmm_fp8_tile_config{0, 0, 0};
-  if ((cfg.bn != 0 && cfg.bn != 256) || cfg.ctas < 0 || cfg.unit_order < 0 || cfg.unit_order > 2)
-    return GMM_ERR_UNSUPPORTED;
   if (!wq || !ws) return GMM_ERR_NULL;
   if (M > 0 && (!xq || !xs || !hq || !hs)) return GMM_ERR_NULL;
   if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(h) || !aligned16(hq) ||
       !aligned16(hs) || !aligned16(group_sizes))
     return GMM_ERR_ALIGN;
+  gmm_fp8_tile_config cfg;
+  if ((st = host_fp8_config(N, 1, config, 0, &cfg)) != GMM_OK) return st;  // the device-independent rules
   if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
   DeviceInfo di;
   if ((st = device_info(&di)) != GMM_OK) return st;
-  if (cfg.ctas > di.sms) return GMM_ERR_UNSUPPORTED;
+  if ((st = host_fp8_config(N, 1, config, di.sms, &cfg)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
   if (M == 0) return GMM_OK;
-
-  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), 1);
-  CUtensorMap map_a, map_b, map_h;
-  if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
-  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
-    return st;
-  // h (when requested) is written through its own tensor map; without h the
-  // kernel stores only hq and hs and never reads map_h
-  if (h) {
-    if ((st = encode_2d(&map_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, N, M, 64, 32)) != GMM_OK) return st;
-  } else {
-    map_h = map_a;
-  }
-  FwdArgs a{};
-  a.xs = xs;
-  a.ws = ws;
-  a.meta = static_cast<const int32_t*>(workspace);
-  a.tiles = reinterpret_cast<const Tile*>(static_cast<const char*>(workspace) + tiles_offset_bytes(G));
-  a.out = static_cast<uint16_t*>(h);
-  a.hq = static_cast<uint8_t*>(hq);
-  a.hs = hs;
-  a.M = static_cast<int>(M);
-  a.K = static_cast<int>(K);
-  a.N = static_cast<int>(N);
-  a.fuse = 1;
-  a.bn = geo.bn_mma;
-  a.col_major = cfg.unit_order == 2 ? 1 : 0;
-  a.wait_limit_ns = wait_limit_ns();
-  const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
-  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
-  const int ctas = cfg.ctas > 0 ? cfg.ctas : di.sms;
-  const int grid = static_cast<int>(max_units < ctas ? max_units : ctas);
-  cudaError_t e = launch_gmm_fp8(map_a, map_b, map_h, a, grid, s);
-  return e == cudaSuccess ? GMM_OK : cuda_fail(e, "gmm_fp8 fused-quant kernel launch");
+  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, 1, h, hq, hs, workspace, cfg, s);
 }
 
 gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes, int G, int64_t M, int64_t K,

@@ -22,6 +22,8 @@ constexpr int kWsNumTiles = 3;
 // finished (the last one resets both to zero for the next launch).
 constexpr int kWsClaimed = 4;
 constexpr int kWsFinished = 5;
+// Number of 256-row tiles (the CTA-pair FP8 kernel's row tiles).
+constexpr int kWsNumPairTiles = 6;
 constexpr int kWsOffsets = 8;
 
 // Row tile height of every grouped kernel (the tcgen05 MMA M).
@@ -37,8 +39,13 @@ __host__ __device__ inline int64_t tiles_offset_bytes(int G) {
 __host__ __device__ inline int64_t order_offset_bytes(int G, int64_t M) {
   return tiles_offset_bytes(G) + 16 * tiles_capacity(G, M);
 }
-__host__ __device__ inline int64_t workspace_bytes(int G, int64_t M) {
+// then the 256-row tiles of every group (the CTA-pair FP8 kernel's tiles)
+__host__ __device__ inline int64_t pair_tiles_capacity(int G, int64_t M) { return (M + 2 * kBM - 1) / (2 * kBM) + G; }
+__host__ __device__ inline int64_t pair_tiles_offset_bytes(int G, int64_t M) {
   return order_offset_bytes(G, M) + ((4 * static_cast<int64_t>(G) + 15) / 16) * 16;
+}
+__host__ __device__ inline int64_t workspace_bytes(int G, int64_t M) {
+  return pair_tiles_offset_bytes(G, M) + 16 * pair_tiles_capacity(G, M);
 }
 
 // Bounded-wait limit handed to every kernel (nanoseconds of %globaltimer).

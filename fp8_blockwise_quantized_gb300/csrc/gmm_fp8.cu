@@ -41,6 +41,7 @@
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "tilewalk.cuh"
 
 namespace gmm {
 
@@ -62,39 +63,6 @@ struct RegSplit {
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kScaleSlots = 8;        // K blocks of scales in flight
 constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
-
-// This CTA's units u = blockIdx.x, + gridDim.x, ...: tile u / per_tile and
-// column block u % per_tile (row-tile major), or tile u % num_tiles and
-// column block u / num_tiles (column-block major).  The next unit's tile is
-// loaded one unit ahead, so its global-memory latency overlaps the current
-// unit instead of sitting between two units on each role's path.  The host
-// keeps the number of units below 2^31, so unit indices are 32-bit.
-struct TileWalk {
-  const Tile* tiles;
-  uint32_t num, u, d;  // d: per_tile (row-tile major) or num_tiles (column-block major)
-  bool col_major;
-  Tile cur, nxt;
-  __device__ TileWalk(const Tile* t, uint32_t per_tile, uint32_t num_units, uint32_t num_tiles, bool column_major)
-      : tiles(t), num(num_units), u(blockIdx.x), d(column_major ? num_tiles : per_tile), col_major(column_major) {
-    if (u < num) cur = load(u);
-    prefetch();
-  }
-  __device__ Tile load(uint32_t v) const {
-    const int4 q = __ldg(reinterpret_cast<const int4*>(tiles + (col_major ? v % d : v / d)));
-    return Tile{q.x, q.y, q.z, q.w};
-  }
-  __device__ void prefetch() {
-    const uint32_t un = u + gridDim.x;
-    if (un < num) nxt = load(un);
-  }
-  __device__ bool live() const { return u < num; }
-  __device__ int col0(int cols) const { return static_cast<int>(col_major ? u / d : u % d) * cols; }
-  __device__ void next() {
-    u += gridDim.x;
-    cur = nxt;
-    prefetch();
-  }
-};
 
 template <int BN, bool FUSE, bool QUANT>
 struct Fp8Tile {
@@ -189,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t c = 0;
       bool ok = true;
-      for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
+      for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
         const Tile tl = w.cur;
         const int n0 = w.col0(C::kOutCols);
         const int brow = tl.g * Nw + n0;
@@ -265,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int NBw = Nw / 128;
     uint32_t q = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int n0 = w.col0(C::kOutCols);
       // the (up to) two RHS column blocks this unit's accumulators use
@@ -298,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ store warp
     uint32_t ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int n0 = w.col0(C::kOutCols);
       if (!__all_sync(0xffffffffu, mbar_wait(staged, ue & 1u, abort_word, lim))) {
@@ -411,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t t = 0, ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major); w.live() && ok; w.next()) {
+    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
       const Tile tl = w.cur;
       const int row = tl.row0 + quad * 32 + lane;
       const bool valid = row < tl.row1;

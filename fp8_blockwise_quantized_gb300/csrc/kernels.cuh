@@ -31,7 +31,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // ---- a1 metadata ------------------------------------------------------------
 __global__ void group_metadata_kernel(const int32_t* sizes, int G, int M, int32_t* ws, Tile* tiles,
-                                      int32_t* order);
+                                      int32_t* order, Tile* pair_tiles);
+// Launches the metadata kernel into a workspace laid out for (G, M).
+cudaError_t launch_group_metadata(const int32_t* sizes, int G, int M, void* workspace, cudaStream_t stream);
 
 // ---- a2 / a3 quantization -----------------------------------------------------
 constexpr int kLhsBlocksPerWarp = 8;
@@ -44,7 +46,8 @@ struct FwdArgs {
   const float* xs;        // fp32 [K/128][M] (FP8 only)
   const float* ws;        // fp32 [G][K/128][Nw/128] (FP8 only)
   const int32_t* meta;    // workspace words
-  const Tile* tiles;      // workspace tile list
+  const Tile* tiles;      // workspace tile list (128-row tiles)
+  const Tile* pair_tiles; // workspace 256-row tiles (CTA-pair FP8 kernel)
   uint16_t* out;          // bf16 [M][N] (may be null with hq)
   uint8_t* hq;            // fused quantized output: e4m3 [M][N] (null: none)
   float* hs;              // fused quantized output scales: fp32 [N/128][M]
@@ -68,6 +71,10 @@ struct TgmmArgs {
 // 32 rows, 128-byte swizzle; read only when args.out is not null.
 cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                            const FwdArgs& args, int grid, cudaStream_t stream);
+// The CTA-pair FP8 kernel: map_b's box is 64 rows (half of a 128-column MMA
+// half); at most max_pairs clusters of two CTAs.
+cudaError_t launch_gmm_fp8_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                                const FwdArgs& args, int max_pairs, cudaStream_t stream);
 cudaError_t launch_gmm_bf16(const CUtensorMap& map_a, const CUtensorMap& map_b, const FwdArgs& args, int grid,
                             cudaStream_t stream);
 // bf16 dgrad: the forward kernel with a K-major weight ([G*N_out, K] view);

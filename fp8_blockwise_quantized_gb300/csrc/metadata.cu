@@ -7,7 +7,8 @@
 //
 // One CTA of 1024 threads: each thread owns a contiguous run of at most
 // ceil(G/1024) groups, the block scans the per-thread row and tile counts, and
-// every thread then writes its groups' offsets and 128-row tiles.
+// every thread then writes its groups' offsets, 128-row tiles and 256-row
+// tiles (the row tiles of the CTA-pair FP8 kernel).
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -52,7 +53,8 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __restrict__ sizes, int G,
                                                                 int M, int32_t* __restrict__ ws,
                                                                 Tile* __restrict__ tiles,
-                                                                int32_t* __restrict__ order) {
+                                                                int32_t* __restrict__ order,
+                                                                Tile* __restrict__ pair_tiles) {
   __shared__ long long warp_sums[33];
   __shared__ unsigned long long keys[kMaxGroups];
   griddep_launch_dependents();
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
   const int per = (G + 1023) / 1024;
   const int g0 = min(G, t * per), g1 = min(G, g0 + per);
 
-  long long rows = 0, ntiles = 0;
+  long long rows = 0, ntiles = 0, npairs = 0;
   int bad = 0;
   for (int g = g0; g < g1; ++g) {
     const int n = sizes[g];
@@ -70,19 +72,21 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
     } else {
       rows += n;
       ntiles += (n + kBM - 1) / kBM;
+      npairs += (n + 2 * kBM - 1) / (2 * kBM);
     }
   }
   const int any_bad = __syncthreads_or(bad);
-  long long rows_total, tiles_total;
+  long long rows_total, tiles_total, pairs_total;
   const long long row_off = block_exclusive_scan(rows, warp_sums, &rows_total);
   const long long tile_off = block_exclusive_scan(ntiles, warp_sums, &tiles_total);
+  const long long pair_off = block_exclusive_scan(npairs, warp_sums, &pairs_total);
 
   int err = 0;
   if (any_bad) err |= kErrNegativeGroup;
   else if (rows_total > M) err |= kErrGroupsExceedM;
 
   if (err == 0) {
-    long long off = row_off, tix = tile_off;
+    long long off = row_off, tix = tile_off, pix = pair_off;
     for (int g = g0; g < g1; ++g) {
       const int n = sizes[g];
       ws[kWsOffsets + g] = static_cast<int>(off);
@@ -93,6 +97,14 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
         tl.row1 = static_cast<int>(off + min(n, r + kBM));
         tl.pad = 0;
         tiles[tix++] = tl;
+      }
+      for (int r = 0; r < n; r += 2 * kBM) {
+        Tile tl;
+        tl.g = g;
+        tl.row0 = static_cast<int>(off + r);
+        tl.row1 = static_cast<int>(off + min(n, r + 2 * kBM));
+        tl.pad = 0;
+        pair_tiles[pix++] = tl;
       }
       off += n;
     }
@@ -121,13 +133,23 @@ __global__ void __launch_bounds__(1024) group_metadata_kernel(const int32_t* __r
       ws[kWsValid] = 0;
       ws[kWsS] = M;
       ws[kWsNumTiles] = 0;
+      ws[kWsNumPairTiles] = 0;
     } else {
       ws[kWsValid] = 1;
       ws[kWsS] = static_cast<int>(rows_total);
       ws[kWsNumTiles] = static_cast<int>(tiles_total);
+      ws[kWsNumPairTiles] = static_cast<int>(pairs_total);
       ws[kWsOffsets + G] = static_cast<int>(rows_total);
     }
   }
+}
+
+cudaError_t launch_group_metadata(const int32_t* sizes, int G, int M, void* workspace, cudaStream_t stream) {
+  char* base = static_cast<char*>(workspace);
+  return launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, stream, sizes, G, M, static_cast<int32_t*>(workspace),
+                    reinterpret_cast<Tile*>(base + tiles_offset_bytes(G)),
+                    reinterpret_cast<int32_t*>(base + order_offset_bytes(G, M)),
+                    reinterpret_cast<Tile*>(base + pair_tiles_offset_bytes(G, M)));
 }
 
 }  // namespace gmm

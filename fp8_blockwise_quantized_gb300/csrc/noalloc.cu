@@ -25,43 +25,31 @@ using namespace gmm;
 
 namespace {
 
-// Static scratch: status word, group offsets and the row-tile list of one
-// call.  64 KiB covers, for example, G <= 1024 groups with M <= 262144 rows;
-// the exact rule is gmm_workspace_bytes(G, M) <= kNoAllocScratchBytes.
+// Static scratch: status word, group offsets and the row-tile lists of one
+// call.  64 KiB covers, for example, G <= 1024 groups with M <= 65536 rows or
+// G <= 256 with M <= 262144; the exact rule is gmm_workspace_bytes(G, M) <=
+// kNoAllocScratchBytes.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 // Per-device set-up, done by the first call on each device with that device
 // current: the device address of the static scratch (in host code the
-// variable's name is only a host-side stand-in, never a device address), the
-// SM count, and the tensor-map encoder.
+// variable's name is only a host-side stand-in, never a device address) and
+// the SM count.
 struct NoAllocDevice {
   void* scratch = nullptr;
   int sms = 0;
   bool ready = false;
 };
 
-gmm_status noalloc_setup(NoAllocDevice* out, EncodeTiledFn* encode) {
+gmm_status noalloc_setup(NoAllocDevice* out) {
   static NoAllocDevice cache[64];
-  static EncodeTiledFn fn = nullptr;
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return host_cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return host_fail(GMM_ERR_UNSUPPORTED, "device ordinal beyond 63");
   std::lock_guard<std::mutex> lk(mu);
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return host_cuda_fail(e, "looking up cuTensorMapEncodeTiled");
-    if (q != cudaDriverEntryPointSuccess) return host_fail(GMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-    fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
   NoAllocDevice& d = cache[dev];
   if (!d.ready) {
     int major = 0, minor = 0, sms = 0;
@@ -79,21 +67,7 @@ gmm_status noalloc_setup(NoAllocDevice* out, EncodeTiledFn* encode) {
     d.ready = true;
   }
   *out = d;
-  *encode = fn;
   return GMM_OK;
-}
-
-gmm_status encode(EncodeTiledFn fn, CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint32_t box_inner, uint32_t box_outer, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                  uint64_t elem_bytes = 1) {
-  cuuint64_t dims[2] = {inner, outer < 1 ? 1 : outer};
-  cuuint64_t strides[1] = {inner * elem_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GMM_OK : host_fail(GMM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 }
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -115,9 +89,12 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   if (!a16(xq) || !a16(xs) || !a16(wq) || !a16(ws) || !a16(out) || !a16(group_sizes)) return GMM_ERR_ALIGN;
 
   NoAllocDevice d;
-  EncodeTiledFn fn = nullptr;
-  gmm_status st = noalloc_setup(&d, &fn);
+  gmm_status st = noalloc_setup(&d);
   if (st != GMM_OK) return st;
+  // the tile configuration gmm_fp8_fwd uses (the defaults), so that both
+  // entry points run the same kernel and give the same bits
+  gmm_fp8_tile_config cfg;
+  if ((st = host_fp8_config(N, fuse, nullptr, d.sms, &cfg)) != GMM_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // The scratch keeps whatever the previous call left; only the sticky error
@@ -125,32 +102,8 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   int32_t* meta = static_cast<int32_t*>(d.scratch);
   cudaError_t e = cudaMemsetAsync(meta + kWsStatus, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return host_cuda_fail(e, "clearing the static scratch's error word");
-  Tile* tiles = reinterpret_cast<Tile*>(static_cast<char*>(d.scratch) + tiles_offset_bytes(G));
-  int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(d.scratch) + order_offset_bytes(G, M));
-  e = launch_pdl(group_metadata_kernel, dim3(1), dim3(1024), 0, s, group_sizes, G, static_cast<int>(M), meta, tiles,
-                 order);
+  e = launch_group_metadata(group_sizes, G, static_cast<int>(M), d.scratch, s);
   if (e != cudaSuccess) return host_cuda_fail(e, "group_metadata_kernel launch");
   if (M == 0) return GMM_OK;
-
-  const Fp8Geometry geo = fp8_geometry(static_cast<int>(N), fuse);
-  CUtensorMap map_a, map_b, map_out;
-  if ((st = encode(fn, &map_a, xq, K, M, 128, 128)) != GMM_OK) return st;
-  if ((st = encode(fn, &map_b, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK) return st;
-  if ((st = encode(fn, &map_out, out, N, M, 64, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2)) != GMM_OK) return st;
-  FwdArgs a{};
-  a.xs = xs;
-  a.ws = ws;
-  a.meta = meta;
-  a.tiles = tiles;
-  a.out = static_cast<uint16_t*>(out);
-  a.M = static_cast<int>(M);
-  a.K = static_cast<int>(K);
-  a.N = static_cast<int>(N);
-  a.fuse = fuse;
-  a.wait_limit_ns = host_wait_limit_ns();
-  const long long max_units = tiles_capacity(G, M) * (N / geo.out_cols);
-  if (max_units >= (1LL << 31)) return GMM_ERR_SHAPE;  // the kernel's unit indices are 32-bit
-  const int grid = static_cast<int>(max_units < d.sms ? max_units : d.sms);
-  e = launch_gmm_fp8(map_a, map_b, map_out, a, grid, s);
-  return e == cudaSuccess ? GMM_OK : host_cuda_fail(e, "gmm_fp8 kernel launch");
+  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, nullptr, nullptr, d.scratch, cfg, s);
 }

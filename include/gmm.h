@@ -89,6 +89,7 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32 word[4], word[5]  set to 0: the work counters of tgmm_bf16 (units
  *                  claimed, CTAs finished); each tgmm_bf16 launch claims its
  *                  units from them and its last CTA sets them back to 0
+ *   int32 word[6]  T2 = number of 256-row tiles (0 when invalid)
  *   int32 word[8 + g], g = 0..G  exclusive prefix sums off_g (off_G = S)
  *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
  *                  every group cut into consecutive tiles of at most 128 rows,
@@ -96,6 +97,9 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32 order[G] at byte offset gmm_tiles_offset(G) + 16 * (ceil(M/128) + G):
  *                  the group ids sorted by size, largest first (ties by id);
  *                  the tgmm kernels take their work largest groups first.
+ *   int32x4 pair_tiles[T2] at byte offset (that of order) + 16 * ceil(G/4):
+ *                  {g, row0, row1, 0} as above with tiles of at most 256
+ *                  rows, the row tiles of the CTA-pair FP8 kernel.
  * The grouped calls below run this step themselves unless they are given
  * group_sizes = NULL, in which case they read what this call (or an earlier
  * grouped call) left in the workspace.
@@ -153,20 +157,30 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
  * ("GEMM Kernel 性能优化十问", Q8: tile sizes chosen by a search over measured
  * candidates, each checked for accuracy).  Every configuration computes the
  * same sums in the same order (each output element is one row tile's K loop
- * of one unit); a field left 0 keeps the default.
- *   bn          columns of W per work unit and MMA N: 128 or 256.  256 needs
- *               N % 256 == 0 (default then); 128 is not available with
- *               fuse_silu_mul = 1, whose units are 256 columns of W.
- *   ctas        persistent CTAs, 1 .. the number of SMs (default: one per SM)
+ * of one unit, every K block's partial promoted in K order); a field left 0
+ * keeps the default.
+ *   bn          columns of W per work unit: 128 or 256.  256 needs
+ *               N % 256 == 0 or fuse_silu_mul = 1 (default then); 128 is not
+ *               available with fuse_silu_mul = 1 or with cta_group = 2.
+ *   ctas        persistent CTAs, 1 .. the number of SMs (default: one per SM,
+ *               rounded down to even for cta_group = 2, which needs an even
+ *               count)
  *   unit_order  1: row-tile major, the column blocks of a row tile run side
  *               by side (default); 2: column-block major, the row tiles that
  *               share a column block of an expert's weights run side by side
+ *   cta_group   1: one CTA per 128-row tile, MMA M = 128, N = bn, two TMEM
+ *               partial buffers (default); 2: CTA pairs on 256-row tiles (the
+ *               MMA of two SMs, M = 256), each K block as two N = 128 halves
+ *               into four TMEM buffers, the weight tile split between the
+ *               pair (needs N % 256 == 0 or fuse_silu_mul = 1, bn 0 or 256
+ *               and an even ctas)
  * A value outside these returns GMM_ERR_UNSUPPORTED before any launch.
  */
 typedef struct {
   int bn;
   int ctas;
   int unit_order;
+  int cta_group;
 } gmm_fp8_tile_config;
 
 /*
@@ -255,7 +269,8 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
  * the library and held until the process exits).  The call allocates nothing:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *   - Limit: gmm_workspace_bytes(G, M) must be <= 65536 (for example G <= 1024
- *     with M <= 262144); larger sizes return GMM_ERR_WORKSPACE and launch
+ *     with M <= 65536, or G <= 256 with M <= 262144); larger sizes return
+ *     GMM_ERR_WORKSPACE and launch
  *     nothing.
  *   - The first call on each device does a one-time set-up with that device
  *     current (it looks up the device address of the array with

@@ -59,7 +59,9 @@ def test_workspace_size(lib):
         assert n >= 32 + 4 * (G + 1) + 16 * tiles
         off = lib.gmm_tiles_offset(G)
         assert off % 16 == 0 and off >= 32 + 4 * (G + 1)
-        assert n == off + 16 * tiles + (4 * G + 15) // 16 * 16  # + the size-ordered group ids
+        pair_tiles = (M + 255) // 256 + G
+        # + the size-ordered group ids, + the 256-row tiles
+        assert n == off + 16 * tiles + (4 * G + 15) // 16 * 16 + 16 * pair_tiles
     assert lib.gmm_workspace_bytes(0, 10) == 0
 
 
@@ -98,6 +100,9 @@ def _tiled(lib, cfg, **kw):
     ((64, 0, 0), {}, 4), ((256, 0, 0), dict(N=384), 4), ((128, 0, 0), dict(fuse=1), 4),
     ((0, -1, 0), {}, 4), ((0, 0, 3), {}, 4), ((0, 0, -1), {}, 4),
     ((256, 0, 2), dict(K=100), 2), ((128, 0, 1), dict(wq=None), 1),
+    # CTA pairs: 256-column units (not with bn 128 or N % 256 != 0), even CTA counts
+    ((0, 0, 0, 2), dict(N=384), 4), ((128, 0, 0, 2), {}, 4), ((0, 7, 0, 2), {}, 4), ((0, 0, 0, 3), {}, 4),
+    ((0, 0, 0, -1), {}, 4),
 ])
 def test_tile_config_host_validation(lib, cfg, kw, code):
     # rejected on the host, before any device call

@@ -83,12 +83,12 @@ def test_fused_quant(sizes, M, K, N):
     _check_against_oracle(x, w, s, h, hq, hs)
 
 
-@pytest.mark.parametrize("ctas,order", [(5, 1), (9, 2), (0, 1)])
-def test_fused_quant_many_units_per_cta(ctas, order):
-    """A mid-size problem with few persistent CTAs, so that every CTA runs
-    dozens of work units back to back: the staging area, its free/staged
-    barriers and the scale ring change phase across units, against the oracle
-    (ctas = 0: one CTA per SM, the default launch)."""
+@pytest.mark.parametrize("ctas,order,cg", [(5, 1, 1), (9, 2, 1), (4, 1, 2), (8, 2, 2), (0, 1, 0)])
+def test_fused_quant_many_units_per_cta(ctas, order, cg):
+    """A mid-size problem with few persistent CTAs (or CTA pairs, cg = 2), so
+    that every CTA runs many work units back to back: the staging area, its
+    free/staged barriers, the TMEM buffers and the scale ring change phase
+    across units, against the oracle (ctas = 0: the default launch)."""
     rng = np.random.default_rng(4000 + ctas)
     G, M, K, N = 9, 4000, 512, 512
     s = rng.multinomial(M - 37, np.full(G, 1.0 / G)).astype(np.int32)
@@ -101,11 +101,12 @@ def test_fused_quant_many_units_per_cta(ctas, order):
     xq, xs = gmm.quantize_lhs(to_dev_bf16(x))
     wq, ws = gmm.quantize_rhs(to_dev_bf16(w))
     g = _guarded_outputs(M_rows, N)
-    cfg = (256, ctas, order) if ctas else None
+    cfg = (256, ctas, order, cg) if ctas else None
     h, hq, hs = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, to_dev(s), out=tuple(b.t for b in g), config=cfg)
     torch.cuda.synchronize()
     for b, what in zip(g, ("h", "hq", "hs")):
         b.check(f"fused quant {what}")
-    units = sum((int(n) + 127) // 128 for n in s) * (N // 128)
-    assert ctas == 0 or units >= 12 * ctas
+    rows_per_tile = 256 if cg == 2 else 128
+    units = sum((int(n) + rows_per_tile - 1) // rows_per_tile for n in s) * (N // 128)
+    assert ctas == 0 or units * (2 if cg == 2 else 1) >= 12 * ctas
     _check_against_oracle(x, w, s, h, hq, hs)

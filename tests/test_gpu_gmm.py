@@ -39,7 +39,7 @@ def _bf16_round(v):
     return oracle.bf16_to_f64(oracle.round_to_bf16(v))
 
 
-def _run_fp8(s, x, w, fuse):
+def _run_fp8(s, x, w, fuse, both_kernels=False):
     M, K = x.shape
     G, _, Nw = w.shape
     N = Nw // 2 if fuse else Nw
@@ -51,6 +51,14 @@ def _run_fp8(s, x, w, fuse):
     torch.cuda.synchronize()
     assert work.status() == 0
     out.check("fp8 fwd output")
+    if both_kernels and (fuse or N % 256 == 0):
+        # the CTA-pair kernel (256-row tiles) gives the default's bits
+        out2 = Guarded((M, N), torch.bfloat16)
+        gmm.fp8_fwd(xq, xs, wq, ws, to_dev(s), fuse=fuse, out=out2.t, workspace=work, config=(0, 0, 0, 2))
+        torch.cuda.synchronize()
+        assert work.status() == 0
+        out2.check("fp8 fwd output, CTA pairs")
+        assert torch.equal(out.t.view(torch.int16), out2.t.view(torch.int16)), "CTA pairs vs one CTA per tile"
     return bf16_to_np64(out.t)
 
 
@@ -66,7 +74,7 @@ def test_fp8_edges(sizes, M, K, N, fuse):
     if fuse and N % 128:
         pytest.skip("fused output needs N % 128 == 0")
     s, x, w = _inputs(sizes, M, K, 2 * N if fuse else N, M + K + N)
-    got = _run_fp8(s, x, w, fuse)
+    got = _run_fp8(s, x, w, fuse, both_kernels=True)
     ref = _oracle_fp8(s, x, w, fuse)
     assert_close(got, ref, FP8_ATOL, FP8_RTOL, "fp8 fwd")
     S = int(s.sum())

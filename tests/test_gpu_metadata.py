@@ -1,5 +1,5 @@
-"""GPU parity of the device metadata kernel (group offsets and the 128-row
-tile list) against the oracle, bit-exact, and its error reporting."""
+"""GPU parity of the device metadata kernel (group offsets, the 128-row and
+256-row tile lists) against the oracle, bit-exact, and its error reporting."""
 import numpy as np
 import pytest
 import torch
@@ -30,6 +30,9 @@ def test_offsets_and_tiles(sizes, M):
     assert hdr[2] == off[-1] and hdr[3] == len(tiles)
     assert ws.offsets() == off.tolist()
     assert np.array_equal(ws.tiles().cpu().numpy(), tiles.astype(np.int32))
+    _, tiles2 = oracle.group_tiles(s, M, 256)
+    assert ws.buf[24:28].view(torch.int32).item() == len(tiles2)
+    assert np.array_equal(ws.pair_tiles().cpu().numpy(), tiles2.astype(np.int32))
     # the group ids by size, largest first, ties by id (numpy's stable sort)
     sz = np.asarray(sizes, np.int64)
     assert ws.order() == np.argsort(-sz, kind="stable").tolist()

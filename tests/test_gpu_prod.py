@@ -94,7 +94,9 @@ def test_prod_forward_chain_sampled(prod):
     h_bits = oracle.round_to_bf16(h_ref)
     ohq, ohs = oracle.quantize_lhs(h_bits)
     y_ref = oracle.gmm_fp8(ohq, ohs, owq_wo, ows_wo, sub)
-    assert_close(bf16_to_np64(y[rsel]), y_ref, FP8_ATOL, FP8_RTOL, "prod wo (sampled rows)")
+    gh_bits = h[rsel].view(torch.int16).cpu().numpy().view(np.uint16)
+    same = (gh_bits.reshape(-1, N // 128, 128) == h_bits.reshape(-1, N // 128, 128)).all(axis=2)
+    _check_wo_rows(bf16_to_np64(y[rsel]), y_ref, same, oracle.bf16_to_f64(h_bits), c, groups, sub, "prod wo")
     # SQNR of the sampled rows against the unquantized fp64 chain, kernel vs oracle
     h_exact = oracle.gmm_bf16(ox, c.w[groups], sub, fuse=True)
     s_k = oracle.sqnr_db(h_exact, bf16_to_np64(h[rsel]))
@@ -127,6 +129,26 @@ def test_prod_tgmm_sampled(layer):
         ref = oracle.tgmm_bf16(np.ascontiguousarray(x[r0:r1][:, ks]), dy[r0:r1], np.array([r1 - r0], np.int32))[0]
         got = bf16_to_np64(dw[g][torch.from_numpy(ks).cuda()])
         assert_close(got, ref, BF16_ATOL, BF16_RTOL, f"prod tgmm {layer} g={g}")
+
+
+def _check_wo_rows(got_y, y_ref, same, hb, c, groups, sub, what):
+    """wo output on sampled rows.  Rows whose FP8 cast of h equals the
+    oracle's in every 1x128 block got the oracle's input: the FP8 bound holds
+    as it stands.  In a row with a block whose h differs by an accumulation-
+    order ulp, that block's cast differs too; each dequantized input then
+    differs by at most the two e4m3 roundings (2^-4 |h| each) plus the h
+    difference (within the FP8 bound), which bounds the change of y by that
+    sum times |W| over the block (|W_q| <= |W| (1 + 2^-4))."""
+    row_same = same.all(axis=1)
+    assert row_same.mean() > 0.5
+    assert_close(got_y[row_same], y_ref[row_same], FP8_ATOL, FP8_RTOL, f"{what} (sampled rows)")
+    off_s = np.concatenate([[0], np.cumsum(sub.astype(np.int64))])
+    g_of_row = np.searchsorted(off_s, np.arange(got_y.shape[0]), side="right") - 1
+    for i in np.flatnonzero(~row_same):
+        dh_max = (2.0 ** -3 * np.abs(hb[i]) + 2 * (FP8_ATOL + FP8_RTOL * np.abs(hb[i]))) * np.repeat(~same[i], 128)
+        w_abs = np.abs(oracle.bf16_to_f64(c.w2[groups[g_of_row[i]]])) * (1 + 2.0 ** -4)
+        bound_y = dh_max @ w_abs + FP8_ATOL + FP8_RTOL * np.abs(y_ref[i])
+        assert np.all(np.abs(got_y[i] - y_ref[i]) <= bound_y), f"{what}, sampled row {i}"
 
 
 def _ref_sampled_chain(c, groups, rows, sub):
@@ -215,9 +237,8 @@ def test_prod_bench_step_sampled(prod):
     bound = np.abs(hb) * 2.0 ** -4 + np.repeat(ghs.astype(np.float64), 128, axis=1) * 2.0 ** -9 + \
         FP8_ATOL + FP8_RTOL * np.abs(hb)
     assert np.all(np.abs(deq - hb) <= bound)
-    # wo on that cast
     got_y = bf16_to_np64(y[rsel])
-    assert_close(got_y, r["y_ref"], FP8_ATOL, FP8_RTOL, "bench step: wo y (sampled rows)")
+    _check_wo_rows(got_y, r["y_ref"], same, hb, c, groups, sub, "bench step: wo y")
     # SQNR against the unquantized fp64 chain: the kernels add no error beyond the method's
     s_wi_k = oracle.sqnr_db(r["h_exact"], got_h)
     s_wi_o = oracle.sqnr_db(r["h_exact"], hb)
@@ -227,13 +248,22 @@ def test_prod_bench_step_sampled(prod):
           f"wo chain kernel {s_wo_k:.2f} / oracle {s_wo_o:.2f} dB")
     assert s_wi_k >= s_wi_o - 0.1
     assert s_wo_k >= s_wo_o - 0.1
-    # tgmm dW_wi = X^T dH (host inputs) on sampled experts and k rows
+    # tgmm dW_wi = X^T dH (host inputs) on sampled experts and k rows.  This
+    # X carries the 1% x50 outliers, so a few dW elements are sums of
+    # thousands of terms that cancel to almost nothing (terms summing to 7000
+    # in absolute value, result 0.1).  Any fp32 accumulator is off there by a
+    # few fp32 units of the terms' absolute sum; the bound adds 2^-18 (64
+    # units) of that sum to the tgmm tolerance.
     ks = np.sort(rng.choice(K, 24, replace=False))
     ks[0], ks[-1] = 0, K - 1
     off = np.concatenate([[0], np.cumsum(c.group_sizes.astype(np.int64))])
     ksel = torch.from_numpy(ks).cuda()
     for g in groups[:6]:
         r0, r1 = off[g], off[g + 1]
-        ref = oracle.tgmm_bf16(np.ascontiguousarray(c.x[r0:r1][:, ks]), dh[r0:r1],
-                               np.array([r1 - r0], np.int32))[0]
-        assert_close(bf16_to_np64(dw_wi[g][ksel]), ref, BF16_ATOL, BF16_RTOL, f"bench step: dW_wi g={g}")
+        xg = np.ascontiguousarray(c.x[r0:r1][:, ks])
+        ref = oracle.tgmm_bf16(xg, dh[r0:r1], np.array([r1 - r0], np.int32))[0]
+        l1 = np.abs(oracle.bf16_to_f64(xg)).T @ np.abs(oracle.bf16_to_f64(dh[r0:r1]))
+        got = bf16_to_np64(dw_wi[g][ksel])
+        bound = BF16_ATOL + BF16_RTOL * np.abs(ref) + 2.0 ** -18 * l1
+        bad = np.abs(got - ref) > bound
+        assert not np.any(bad), f"bench step: dW_wi g={g}: {int(bad.sum())} elements out of tolerance"

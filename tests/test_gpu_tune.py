@@ -36,6 +36,10 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+def _even(n):
+    return n - n % 2
+
+
 @pytest.mark.parametrize("sizes,M,K,N", CASES)
 def test_every_config_gives_the_default_bits(sizes, M, K, N):
     s, xq, xs, wq, ws = _problem(sizes, M, K, N, 5 + M)
@@ -45,23 +49,30 @@ def test_every_config_gives_the_default_bits(sizes, M, K, N):
     for bn in bns:
         for ctas in (0, 1, 7, sms // 2, sms):
             for order in (1, 2):
-                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(bn, ctas, order))
-                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (bn, ctas, order)
+                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(bn, ctas, order, 1))
+                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (bn, ctas, order, 1)
+    if N % 256 == 0:  # CTA pairs: 256-column units, an even CTA count
+        for ctas in (0, 2, 8, _even(sms // 2), sms):
+            for order in (1, 2):
+                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(256, ctas, order, 2))
+                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (256, ctas, order, 2)
 
 
 def test_fused_configs_give_the_default_bits():
     sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
     s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 17)
     ref = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True)
-    for ctas in (0, 3, _sms() // 2):
-        for order in (1, 2):
-            got = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(256, ctas, order))
-            assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (ctas, order)
+    for cg, ctas_list in ((1, (0, 3, _sms() // 2)), (2, (0, 2, _even(_sms() // 2)))):
+        for ctas in ctas_list:
+            for order in (1, 2):
+                got = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(256, ctas, order, cg))
+                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (ctas, order, cg)
 
 
 def test_config_errors_on_the_device():
     s, xq, xs, wq, ws = _problem([100, 28], 128, 256, 384, 3)
-    for cfg in [(256, 0, 1), (0, _sms() + 1, 1), (64, 0, 1), (0, 0, 3)]:
+    # N = 384: no 256-column units (bn 256, CTA pairs); bad counts and values
+    for cfg in [(256, 0, 1), (0, _sms() + 1, 1), (64, 0, 1), (0, 0, 3), (0, 0, 1, 2), (0, 0, 1, 3)]:
         with pytest.raises(gmm.GmmError) as e:
             gmm.fp8_fwd(xq, xs, wq, ws, s, config=cfg)
         assert e.value.status == 4, cfg
@@ -69,6 +80,10 @@ def test_config_errors_on_the_device():
     s, xq, xs, wq, ws = _problem([100, 28], 128, 256, 512, 4)
     with pytest.raises(gmm.GmmError) as e:
         gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(128, 0, 1))
+    assert e.value.status == 4
+    # CTA pairs need an even CTA count
+    with pytest.raises(gmm.GmmError) as e:
+        gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(256, 7, 1, 2))
     assert e.value.status == 4
 
 
@@ -91,11 +106,12 @@ def test_fused_cast_configs_give_the_default_bits():
     sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
     s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 29)
     ref = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s)
-    for ctas in (0, 5, _sms() // 2):
-        for order in (1, 2):
-            got = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(256, ctas, order))
-            for a, b in zip(ref, got):
-                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (ctas, order)
+    for cg, ctas_list in ((1, (0, 5, _sms() // 2)), (2, (0, 4, _even(_sms() // 2)))):
+        for ctas in ctas_list:
+            for order in (1, 2):
+                got = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(256, ctas, order, cg))
+                for a, b in zip(ref, got):
+                    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (ctas, order, cg)
     with pytest.raises(gmm.GmmError) as e:
         gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(128, 0, 1))
     assert e.value.status == 4
