@@ -11,7 +11,8 @@ e4m3 codes as ``numpy.uint8``.
 
 Layouts are the method's natural ones (not the CUDA library's):
   xq [M, K] uint8, xs [M, K/128] float32                 (1x128 LHS blocks)
-  wq [G, K, N] uint8, ws [G, K/128, N/128] float32        (128x128 RHS blocks)
+  wq [G, K, N] uint8, ws [G, K/128, N/128] float32        (128x128 RHS blocks;
+      e4m3 codes, or e2m1 codes one per byte for the 4-bit weights)
 """
 from __future__ import annotations
 
@@ -66,6 +67,14 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_e4m3_encode_array.argtypes = [P, I64, P]
         lib.oracle_e4m3_decode_array.argtypes = [P, I64, P]
+        lib.oracle_e2m1_decode.restype = ctypes.c_double
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_encode_array.argtypes = [P, I64, P]
+        lib.oracle_e2m1_decode_array.argtypes = [P, I64, P]
+        lib.oracle_quantize_rhs_e2m1.argtypes = [P, I64, I64, I64, P, P]
+        lib.oracle_gmm_fp8_w4.argtypes = [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, P]
         lib.oracle_round_to_bf16.restype = ctypes.c_uint16
         lib.oracle_round_to_bf16.argtypes = [ctypes.c_double]
         lib.oracle_round_to_bf16_array.argtypes = [P, I64, P]
@@ -128,6 +137,22 @@ def e4m3_encode(values) -> np.ndarray:
     return out
 
 
+def e2m1_decode(codes) -> np.ndarray:
+    """FP4 E2M1 value of each code (the low 4 bits of each byte)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e2m1_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e2m1_encode(values) -> np.ndarray:
+    """FP4 E2M1 code (0..15) of each fp32 value: nearest, ties to even, saturating at 6."""
+    v = _c(values, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
 def round_to_bf16(values) -> np.ndarray:
     """fp64 -> fp32 (nearest) -> bf16 (nearest, ties to even), as uint16 bits."""
     v = _c(values, np.float64)
@@ -168,6 +193,17 @@ def quantize_rhs(w_bf16) -> tuple[np.ndarray, np.ndarray]:
     wq = np.empty((G, K, N), np.uint8)
     ws = np.empty((G, K // 128, N // 128), np.float32)
     _check(_load().oracle_quantize_rhs(_ptr(w), G, K, N, _ptr(wq), _ptr(ws)))
+    return wq, ws
+
+
+def quantize_rhs_e2m1(w_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """4-bit weights: 128x128 blocks, scale = absmax / 6, e2m1 codes ->
+    (wq [G,K,N] u8, one code per byte; ws [G,K/128,N/128] f32)."""
+    w = _c(w_bf16, np.uint16)
+    G, K, N = w.shape
+    wq = np.empty((G, K, N), np.uint8)
+    ws = np.empty((G, K // 128, N // 128), np.float32)
+    _check(_load().oracle_quantize_rhs_e2m1(_ptr(w), G, K, N, _ptr(wq), _ptr(ws)))
     return wq, ws
 
 
@@ -212,6 +248,24 @@ def gmm_fp8(xq, xs, wq, ws, group_sizes, fuse: bool = False) -> np.ndarray:
     out = np.empty((M, N), np.float64)
     _check(_load().oracle_gmm_fp8(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(s), G, M, K, N,
                                   int(bool(fuse)), _ptr(out)))
+    return out
+
+
+def gmm_fp8_w4(xq, xs, wq4, ws, group_sizes, fuse: bool = False) -> np.ndarray:
+    """gmm_fp8 with e2m1 weight codes (one per byte, [G, K, Nw]) and their
+    128x128 scales; the activations stay e4m3 in 1x128 blocks."""
+    xq = _c(xq, np.uint8)
+    xs = _c(xs, np.float32)
+    wq4 = _c(wq4, np.uint8)
+    ws = _c(ws, np.float32)
+    s = _c(group_sizes, np.int32)
+    M, K = xq.shape
+    G, K2, Nw = wq4.shape
+    assert K2 == K and s.size == G
+    N = Nw // 2 if fuse else Nw
+    out = np.empty((M, N), np.float64)
+    _check(_load().oracle_gmm_fp8_w4(_ptr(xq), _ptr(xs), _ptr(wq4), _ptr(ws), _ptr(s), G, M, K, N,
+                                     int(bool(fuse)), _ptr(out)))
     return out
 
 

@@ -14,6 +14,8 @@
  * Sources (page title, section):
  *  [Q1..Q9]  "GEMM Kernel 性能优化十问" (pengchengneo.github.io), questions 1-9.
  *  [V2 3.3]  "实现差距：GMM Kernel（V1 vs V2）", §3.3 动态 LHS 量化.
+ *  [V2 3.4]  same page, §3.4 Sub-byte 类型支持 (int4 / float4_e2m1fn weights,
+ *            the blockwise fp32-scale arithmetic otherwise unchanged).
  *  [V2 3.5]  same page, §3.5 激活函数融合 (fused gate/up activation).
  *  [V2 3.6]  same page, §3.6 异步 DMA 置零 (zeroing the uncovered output).
  *  [MoE 1]   "MoE 优化的探索", §1 (SwiGLU expert: z = SiLU(g) * u).
@@ -167,9 +169,9 @@ void oracle_e4m3_decode_array(const uint8_t *c, int64_t n, double *out)
 /* read as IEEE binary32 (the scale is stored as fp32).                      */
 /* ------------------------------------------------------------------------ */
 
-static void quantize_block_scale(float absmax, float *scale, float *inv)
+static void quantize_block_scale(float absmax, float dtype_max, float *scale, float *inv)
 {
-    volatile float s = absmax / 448.0f; /* volatile: keep it one fp32 divide */
+    volatile float s = absmax / dtype_max; /* volatile: keep it one fp32 divide */
     *scale = s;
     *inv = (s == 0.0f) ? 0.0f : 1.0f / s;
 }
@@ -193,7 +195,7 @@ int oracle_quantize_lhs(const uint16_t *x, int64_t M, int64_t K, uint8_t *xq, fl
                     absmax = a;
             }
             float s, inv;
-            quantize_block_scale(absmax, &s, &inv);
+            quantize_block_scale(absmax, 448.0f, &s, &inv);
             xs[m * KB + kb] = s;
             for (int j = 0; j < 128; ++j) {
                 volatile float prod = bf16_bits_to_float(blk[j]) * inv;
@@ -225,12 +227,99 @@ int oracle_quantize_rhs(const uint16_t *w, int64_t G, int64_t K, int64_t N, uint
                             absmax = a;
                     }
                 float s, inv;
-                quantize_block_scale(absmax, &s, &inv);
+                quantize_block_scale(absmax, 448.0f, &s, &inv);
                 ws[(g * KB + kb) * NB + nb] = s;
                 for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
                     for (int64_t n = nb * 128; n < nb * 128 + 128; ++n) {
                         volatile float prod = bf16_bits_to_float(w[(g * K + k) * N + n]) * inv;
                         wq[(g * K + k) * N + n] = e4m3_encode_with(table, prod);
+                    }
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP4 E2M1 codec, from the format definition (OCP MX FP4): 1 sign bit, 2   */
+/* exponent bits (bias 1), 1 mantissa bit; no infinities and no NaN; the     */
+/* largest magnitude is 6; exponent field 0 is subnormal, value m/2.  A code */
+/* is the low 4 bits of a byte.  [V2 3.4] names float4_e2m1fn as a weight   */
+/* type; the cast is read as round-to-nearest, ties to even, saturating at 6.*/
+/* ------------------------------------------------------------------------ */
+
+double oracle_e2m1_decode(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double mag = (e == 0) ? 0.5 * (double)m : (1.0 + 0.5 * (double)m) * ldexp(1.0, e - 1);
+    return sign ? -mag : mag;
+}
+
+/* nearest of the 8 magnitudes; an exact tie goes to the even code */
+static uint8_t e2m1_encode_value(float v)
+{
+    uint8_t sign = (signbit(v) ? 0x8 : 0x0);
+    double a = fabs((double)v);
+    if (a >= 6.0)
+        return (uint8_t)(sign | 0x7);
+    int best = 0;
+    double best_err = a;
+    for (int c = 1; c <= 7; ++c) {
+        double err = fabs(oracle_e2m1_decode((uint8_t)c) - a);
+        if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_err = err;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+uint8_t oracle_e2m1_encode(float v)
+{
+    return e2m1_encode_value(v);
+}
+
+void oracle_e2m1_encode_array(const float *v, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e2m1_encode_value(v[i]);
+}
+
+void oracle_e2m1_decode_array(const uint8_t *c, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e2m1_decode(c[i]);
+}
+
+/* 4-bit weights [V2 3.4]: the 128x128 block rule of [Q2] with the 4-bit
+ * type's largest value as dtype_max: scale = absmax / 6, inv = 0 where scale
+ * == 0 else 1/scale, code = e2m1(w * inv).  wq: one code per byte, [G][K][N]
+ * (the natural layout, like oracle_quantize_rhs); ws: fp32 [G][K/128][N/128]. */
+int oracle_quantize_rhs_e2m1(const uint16_t *w, int64_t G, int64_t K, int64_t N, uint8_t *wq, float *ws)
+{
+    if (G <= 0 || K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0)
+        return OR_ERR_SHAPE;
+    int64_t KB = K / 128, NB = N / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t g = 0; g < G; ++g) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            for (int64_t nb = 0; nb < NB; ++nb) {
+                float absmax = 0.0f;
+                for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
+                    for (int64_t n = nb * 128; n < nb * 128 + 128; ++n) {
+                        float a = fabsf(bf16_bits_to_float(w[(g * K + k) * N + n]));
+                        if (a > absmax)
+                            absmax = a;
+                    }
+                float s, inv;
+                quantize_block_scale(absmax, 6.0f, &s, &inv);
+                ws[(g * KB + kb) * NB + nb] = s;
+                for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
+                    for (int64_t n = nb * 128; n < nb * 128 + 128; ++n) {
+                        volatile float prod = bf16_bits_to_float(w[(g * K + k) * N + n]) * inv;
+                        wq[(g * K + k) * N + n] = e2m1_encode_value(prod);
                     }
             }
         }
@@ -316,9 +405,11 @@ static int64_t group_of_row(const int64_t *offsets, int64_t G, int64_t m)
     return -1;
 }
 
-int oracle_gmm_fp8(const uint8_t *xq, const float *xs, const uint8_t *wq, const float *ws,
-                   const int32_t *sizes, int64_t G, int64_t M, int64_t K, int64_t N, int fuse,
-                   double *out)
+/* wdec: the value of every weight code byte (e4m3, or e2m1 for 4-bit
+ * weights); the activation codes are e4m3. */
+static int gmm_blockwise(const uint8_t *xq, const float *xs, const uint8_t *wq, const float *ws,
+                         const int32_t *sizes, int64_t G, int64_t M, int64_t K, int64_t N, int fuse,
+                         const double *wdec, double *out)
 {
     if (G <= 0 || M < 0 || K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0)
         return OR_ERR_SHAPE;
@@ -355,7 +446,7 @@ int oracle_gmm_fp8(const uint8_t *xq, const float *xs, const uint8_t *wq, const 
                     double a = dec[xq[m * K + k]];
                     const uint8_t *wrow = wq + (g * K + k) * Nw;
                     for (int64_t n = 0; n < Nw; ++n)
-                        part[n] += a * dec[wrow[n]];
+                        part[n] += a * wdec[wrow[n]];
                 }
                 double sx = (double)xs[m * KB + kb];
                 for (int64_t n = 0; n < Nw; ++n) {
@@ -371,6 +462,29 @@ int oracle_gmm_fp8(const uint8_t *xq, const float *xs, const uint8_t *wq, const 
     }
     free(offsets);
     return OR_OK;
+}
+
+int oracle_gmm_fp8(const uint8_t *xq, const float *xs, const uint8_t *wq, const float *ws,
+                   const int32_t *sizes, int64_t G, int64_t M, int64_t K, int64_t N, int fuse,
+                   double *out)
+{
+    double wdec[256];
+    for (int c = 0; c < 256; ++c)
+        wdec[c] = oracle_e4m3_decode((uint8_t)c);
+    return gmm_blockwise(xq, xs, wq, ws, sizes, G, M, K, N, fuse, wdec, out);
+}
+
+/* 4-bit weights [V2 3.4]: the same forward with e2m1 weight codes (one code
+ * per byte, [G][K][Nw]) and their 128x128 fp32 scales; the activations stay
+ * e4m3 in 1x128 blocks. */
+int oracle_gmm_fp8_w4(const uint8_t *xq, const float *xs, const uint8_t *wq, const float *ws,
+                      const int32_t *sizes, int64_t G, int64_t M, int64_t K, int64_t N, int fuse,
+                      double *out)
+{
+    double wdec[256];
+    for (int c = 0; c < 256; ++c)
+        wdec[c] = (c < 16) ? oracle_e2m1_decode((uint8_t)c) : NAN;
+    return gmm_blockwise(xq, xs, wq, ws, sizes, G, M, K, N, fuse, wdec, out);
 }
 
 /* ------------------------------------------------------------------------ */
