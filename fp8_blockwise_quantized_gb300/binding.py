@@ -30,7 +30,8 @@ EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "
             "gmm_group_metadata", "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_fp8_fwd",
             "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
             "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_tiled",
-            "gmm_fp8_fwd_swiglu_quant_tiled"]
+            "gmm_fp8_fwd_swiglu_quant_tiled", "gmm_quantize_rhs_w4", "gmm_fp8_w4_fwd",
+            "gmm_fp8_w4_fwd_swiglu_quant"]
 
 
 class TileConfig(ctypes.Structure):
@@ -104,6 +105,13 @@ def load():
     lib.gmm_selftest_wait_timeout.argtypes = [P, SZ, I, P]
     lib.gmm_fp8_fwd_noalloc.restype = I
     lib.gmm_fp8_fwd_noalloc.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P]
+    lib.gmm_quantize_rhs_w4.restype = I
+    lib.gmm_quantize_rhs_w4.argtypes = [P, I, I64, I64, P, P, P]
+    lib.gmm_fp8_w4_fwd.restype = I
+    lib.gmm_fp8_w4_fwd.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, P, P, SZ, P, ctypes.POINTER(TileConfig)]
+    lib.gmm_fp8_w4_fwd_swiglu_quant.restype = I
+    lib.gmm_fp8_w4_fwd_swiglu_quant.argtypes = [P, P, P, P, P, I, I64, I64, I64, P, P, P, P, SZ, P,
+                                                ctypes.POINTER(TileConfig)]
     _lib = lib
     return lib
 
@@ -183,6 +191,31 @@ def gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, h
     return load().gmm_fp8_fwd_swiglu_quant_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
                                                  _p(h), _p(hq), _p(hs), _p(workspace), workspace_bytes, _s(stream),
                                                  ctypes.byref(config) if config is not None else None)
+
+
+def _cfg(config):
+    if config is None:
+        return None
+    if not isinstance(config, TileConfig):
+        config = TileConfig(*config)
+    return ctypes.byref(config)
+
+
+def gmm_quantize_rhs_w4(w, G, K, N, wq4, ws, stream=None) -> int:
+    return load().gmm_quantize_rhs_w4(_p(w), G, K, N, _p(wq4), _p(ws), _s(stream))
+
+
+def gmm_fp8_w4_fwd(xq, xs, wq4, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, workspace_bytes,
+                   stream=None, config=None) -> int:
+    return load().gmm_fp8_w4_fwd(_p(xq), _p(xs), _p(wq4), _p(ws), _p(group_sizes), G, M, K, N, int(fuse_silu_mul),
+                                 _p(out), _p(workspace), workspace_bytes, _s(stream), _cfg(config))
+
+
+def gmm_fp8_w4_fwd_swiglu_quant(xq, xs, wq4, ws, group_sizes, G, M, K, N, h, hq, hs, workspace, workspace_bytes,
+                                stream=None, config=None) -> int:
+    return load().gmm_fp8_w4_fwd_swiglu_quant(_p(xq), _p(xs), _p(wq4), _p(ws), _p(group_sizes), G, M, K, N, _p(h),
+                                              _p(hq), _p(hs), _p(workspace), workspace_bytes, _s(stream),
+                                              _cfg(config))
 
 
 def gmm_bf16_fwd(x, w, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, workspace_bytes,
@@ -293,6 +326,48 @@ def quantize_rhs(w: torch.Tensor, stream=None):
     ws = torch.empty((G, K // 128, N // 128), dtype=torch.float32, device=w.device)
     _check(gmm_quantize_rhs(w, G, K, N, wq, ws, stream), "gmm_quantize_rhs")
     return wq, ws
+
+
+def quantize_rhs_w4(w: torch.Tensor, stream=None):
+    """w bf16 [G, K, N] -> (wq4 uint8 [G, N, K/2] packed E2M1 codes, ws float32 [G, K/128, N/128])."""
+    G, K, N = w.shape
+    wq4 = torch.empty((G, N, K // 2), dtype=torch.uint8, device=w.device)
+    ws = torch.empty((G, K // 128, N // 128), dtype=torch.float32, device=w.device)
+    _check(gmm_quantize_rhs_w4(w, G, K, N, wq4, ws, stream), "gmm_quantize_rhs_w4")
+    return wq4, ws
+
+
+def fp8_w4_fwd(xq, xs, wq4, ws, group_sizes, fuse=False, out=None, workspace=None, stream=None, config=None):
+    """The FP8 forward with 4-bit weights (wq4 [G, Nw, K/2] from quantize_rhs_w4)."""
+    M, K = xq.shape
+    G, Nw, K2 = wq4.shape
+    assert 2 * K2 == K
+    N = Nw // 2 if fuse else Nw
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
+    _check(gmm_fp8_w4_fwd(xq, xs, wq4, ws, group_sizes, G, M, K, N, fuse, out, ws_.buf, ws_.nbytes, stream, config),
+           "gmm_fp8_w4_fwd")
+    return out
+
+
+def fp8_w4_fwd_swiglu_quant(xq, xs, wq4, ws, group_sizes, with_h=True, workspace=None, stream=None, config=None,
+                            out=None):
+    """Fused wi with 4-bit weights: returns (h or None, hq, hs) as fp8_fwd_swiglu_quant."""
+    M, K = xq.shape
+    G, Nw, K2 = wq4.shape
+    assert 2 * K2 == K
+    N = Nw // 2
+    if out is not None:
+        h, hq, hs = out
+    else:
+        h = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if with_h else None
+        hq = torch.empty((M, N), dtype=torch.uint8, device=xq.device)
+        hs = torch.empty((N // 128, M), dtype=torch.float32, device=xq.device)
+    ws_ = _ws_for(group_sizes, workspace, G, M, xq.device)
+    _check(gmm_fp8_w4_fwd_swiglu_quant(xq, xs, wq4, ws, group_sizes, G, M, K, N, h, hq, hs, ws_.buf, ws_.nbytes,
+                                       stream, config), "gmm_fp8_w4_fwd_swiglu_quant")
+    return h, hq, hs
 
 
 def fp8_fwd(xq, xs, wq, ws, group_sizes, fuse=False, out=None, workspace=None, stream=None, config=None):

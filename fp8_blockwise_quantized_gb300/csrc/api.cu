@@ -124,6 +124,34 @@ gmm_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, c
   return GMM_OK;
 }
 
+// Tensor map of packed 4-bit weight codes: `rows` rows of K codes (K/2 bytes),
+// boxes of 128 codes x box_rows rows, each 16 codes landing in 16 bytes of
+// shared memory (the 4-bit MMA operand layout), 128-byte swizzle.  The base
+// must be 32-byte aligned and K a multiple of 128 (the rows' stride a
+// multiple of 32 bytes).
+gmm_status encode_2d_w4(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    std::snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled is not available");
+    return GMM_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {K, rows < 1 ? 1 : rows};
+  cuuint64_t strides[1] = {K / 2};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_last_error, sizeof g_last_error, "cuTensorMapEncodeTiled (4-bit weights) failed (%d)",
+                  static_cast<int>(r));
+    return GMM_ERR_CUDA;
+  }
+  return GMM_OK;
+}
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 // Shape checks shared by the grouped calls.
 gmm_status check_grouped(int G, int64_t M, int64_t K, int64_t N, int64_t Nw) {
   if (G < 1 || G > kMaxGroups) return GMM_ERR_SHAPE;
@@ -145,6 +173,19 @@ gmm_status check_workspace(const void* workspace, size_t bytes, int G, int64_t M
   if (bytes < static_cast<size_t>(workspace_bytes(G, M))) return GMM_ERR_WORKSPACE;
   return GMM_OK;
 }
+
+}  // namespace
+
+namespace {
+
+// The FP8 forward entry points: argument checks (all before any launch),
+// the group metadata unless group_sizes is NULL, then the launch.  quant: the
+// fused gate/up forward that also writes its output's 1x128 FP8 cast (hq, hs;
+// out = h may be NULL); w4: 4-bit E2M1 weight codes, packed.
+gmm_status fp8_entry(const void* xq, const float* xs, const void* wq, const float* ws, const int32_t* group_sizes,
+                     int G, int64_t M, int64_t K, int64_t N, int fuse, void* out, void* hq, float* hs, bool quant,
+                     void* workspace, size_t workspace_bytes, void* stream, const gmm_fp8_tile_config* config,
+                     int w4);
 
 }  // namespace
 
@@ -182,7 +223,7 @@ gmm_status host_fp8_config(int64_t N, int fuse, const gmm_fp8_tile_config* in, i
 
 gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, const float* ws, int G, int64_t M,
                            int64_t K, int64_t N, int fuse, void* out, void* hq, float* hs, void* workspace,
-                           const gmm_fp8_tile_config& cfg, cudaStream_t s) {
+                           const gmm_fp8_tile_config& cfg, cudaStream_t s, int w4) {
   const bool pair = cfg.cta_group == 2;
   const int64_t Nw = fuse ? 2 * N : N;
   // MMA N per unit, output columns per unit, rows of the weight tensor-map box
@@ -190,8 +231,14 @@ gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, cons
   CUtensorMap map_a, map_b, map_out;
   gmm_status st;
   if ((st = encode_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, xq, K, M, 128, 128)) != GMM_OK) return st;
-  if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) != GMM_OK)
+  if (w4) {
+    // packed 4-bit codes [G*Nw][K/2] bytes, expanded by the copy into the
+    // shared-memory layout of 4-bit MMA operands (16 codes in each 16 bytes)
+    if ((st = encode_2d_w4(&map_b, wq, K, G * Nw, geo.b_box_rows)) != GMM_OK) return st;
+  } else if ((st = encode_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, wq, K, G * Nw, 128, geo.b_box_rows)) !=
+             GMM_OK) {
     return st;
+  }
   // the bf16 output is written through its own tensor map; the fused cast
   // without h stores only hq and hs and never reads map_out
   if (out) {
@@ -214,6 +261,7 @@ gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, cons
   a.fuse = fuse;
   a.bn = geo.bn_mma;
   a.col_major = cfg.unit_order == 2 ? 1 : 0;
+  a.b_fmt = w4 ? 5 : 0;  // kind::f8f6f4 operand types: e2m1 or e4m3
   a.wait_limit_ns = host_wait_limit_ns();
   const long long tiles = pair ? pair_tiles_capacity(G, M) : tiles_capacity(G, M);
   const long long max_units = tiles * (N / geo.out_cols);
@@ -229,6 +277,38 @@ gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, cons
 }
 
 }  // namespace gmm
+
+namespace {
+
+gmm_status fp8_entry(const void* xq, const float* xs, const void* wq, const float* ws, const int32_t* group_sizes,
+                     int G, int64_t M, int64_t K, int64_t N, int fuse, void* out, void* hq, float* hs, bool quant,
+                     void* workspace, size_t workspace_bytes, void* stream, const gmm_fp8_tile_config* config,
+                     int w4) {
+  const int64_t Nw = fuse ? 2 * N : N;
+  gmm_status st = check_grouped(G, M, K, N, Nw);
+  if (st != GMM_OK) return st;
+  if (!wq || !ws) return GMM_ERR_NULL;
+  if (M > 0 && (!xq || !xs)) return GMM_ERR_NULL;
+  if (M > 0 && (quant ? (!hq || !hs) : !out)) return GMM_ERR_NULL;
+  if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(out) ||
+      !aligned16(hq) || !aligned16(hs) || !aligned16(group_sizes))
+    return GMM_ERR_ALIGN;
+  if (w4 && !aligned32(wq)) return GMM_ERR_ALIGN;  // the 4-bit tensor map's base
+  gmm_fp8_tile_config cfg;
+  if ((st = host_fp8_config(N, fuse, config, 0, &cfg)) != GMM_OK) return st;  // the device-independent rules
+  if (quant && cfg.bn != 256) return GMM_ERR_UNSUPPORTED;
+  if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
+  DeviceInfo di;
+  if ((st = device_info(&di)) != GMM_OK) return st;
+  if ((st = host_fp8_config(N, fuse, config, di.sms, &cfg)) != GMM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
+  if (M == 0) return GMM_OK;
+  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, quant ? hq : nullptr, quant ? hs : nullptr,
+                         workspace, cfg, s, w4);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -304,64 +384,63 @@ gmm_status gmm_quantize_rhs(const void* w, int G, int64_t K, int64_t N, void* wq
 gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const float* ws, const int32_t* group_sizes,
                        int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul, void* out, void* workspace,
                        size_t workspace_bytes, void* stream) {
-  return gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace, workspace_bytes,
-                           stream, nullptr);
+  return fp8_entry(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul ? 1 : 0, out, nullptr, nullptr, false,
+                   workspace, workspace_bytes, stream, nullptr, 0);
 }
 
 gmm_status gmm_fp8_fwd_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
                              const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul,
                              void* out, void* workspace, size_t workspace_bytes, void* stream,
                              const gmm_fp8_tile_config* config) {
-  const int fuse = fuse_silu_mul ? 1 : 0;
-  const int64_t Nw = fuse ? 2 * N : N;
-  gmm_status st = check_grouped(G, M, K, N, Nw);
-  if (st != GMM_OK) return st;
-  if (!wq || !ws) return GMM_ERR_NULL;
-  if (M > 0 && (!xq || !xs || !out)) return GMM_ERR_NULL;
-  if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(out) ||
-      !aligned16(group_sizes))
-    return GMM_ERR_ALIGN;
-  gmm_fp8_tile_config cfg;
-  if ((st = host_fp8_config(N, fuse, config, 0, &cfg)) != GMM_OK) return st;  // the device-independent rules
-  if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
-  DeviceInfo di;
-  if ((st = device_info(&di)) != GMM_OK) return st;
-  if ((st = host_fp8_config(N, fuse, config, di.sms, &cfg)) != GMM_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
-  if (M == 0) return GMM_OK;
-  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, nullptr, nullptr, workspace, cfg, s);
+  return fp8_entry(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul ? 1 : 0, out, nullptr, nullptr, false,
+                   workspace, workspace_bytes, stream, config, 0);
 }
 
 gmm_status gmm_fp8_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq, const float* ws,
                                     const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
                                     void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream) {
-  return gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
-                                        workspace_bytes, stream, nullptr);
+  return fp8_entry(xq, xs, wq, ws, group_sizes, G, M, K, N, 1, h, hq, hs, true, workspace, workspace_bytes, stream,
+                   nullptr, 0);
 }
 
 gmm_status gmm_fp8_fwd_swiglu_quant_tiled(const void* xq, const float* xs, const void* wq, const float* ws,
                                           const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N,
                                           void* h, void* hq, float* hs, void* workspace, size_t workspace_bytes,
                                           void* stream, const gmm_fp8_tile_config* config) {
-  const int64_t Nw = 2 * N;
-  gmm_status st = check_grouped(G, M, K, N, Nw);
-  if (st != GMM_OK) return st;
-  if (!wq || !ws) return GMM_ERR_NULL;
-  if (M > 0 && (!xq || !xs || !hq || !hs)) return GMM_ERR_NULL;
-  if (!aligned16(wq) || !aligned16(ws) || !aligned16(xq) || !aligned16(xs) || !aligned16(h) || !aligned16(hq) ||
-      !aligned16(hs) || !aligned16(group_sizes))
-    return GMM_ERR_ALIGN;
-  gmm_fp8_tile_config cfg;
-  if ((st = host_fp8_config(N, 1, config, 0, &cfg)) != GMM_OK) return st;  // the device-independent rules
-  if ((st = check_workspace(workspace, workspace_bytes, G, M)) != GMM_OK) return st;
+  return fp8_entry(xq, xs, wq, ws, group_sizes, G, M, K, N, 1, h, hq, hs, true, workspace, workspace_bytes, stream,
+                   config, 0);
+}
+
+gmm_status gmm_quantize_rhs_w4(const void* w, int G, int64_t K, int64_t N, void* wq4, float* ws, void* stream) {
+  if (G < 1 || K < 128 || K % 128 != 0 || N < 128 || N % 128 != 0 || K > (1 << 24) || N > (1 << 24))
+    return GMM_ERR_SHAPE;
+  if (static_cast<int64_t>(G) * (K / 128) * (N / 128) > INT32_MAX) return GMM_ERR_SHAPE;
+  if (!w || !wq4 || !ws) return GMM_ERR_NULL;
+  if (!aligned16(w) || !aligned32(wq4) || !aligned16(ws)) return GMM_ERR_ALIGN;
   DeviceInfo di;
-  if ((st = device_info(&di)) != GMM_OK) return st;
-  if ((st = host_fp8_config(N, 1, config, di.sms, &cfg)) != GMM_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (group_sizes && (st = launch_metadata(group_sizes, G, M, workspace, s)) != GMM_OK) return st;
-  if (M == 0) return GMM_OK;
-  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, 1, h, hq, hs, workspace, cfg, s);
+  gmm_status st = device_info(&di);
+  if (st != GMM_OK) return st;
+  const int grid = static_cast<int>(static_cast<int64_t>(G) * (K / 128) * (N / 128));
+  quantize_rhs_w4_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(w), static_cast<int>(K), static_cast<int>(N), static_cast<uint8_t*>(wq4), ws);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GMM_OK : cuda_fail(e, "quantize_rhs_w4_kernel launch");
+}
+
+gmm_status gmm_fp8_w4_fwd(const void* xq, const float* xs, const void* wq4, const float* ws,
+                          const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul,
+                          void* out, void* workspace, size_t workspace_bytes, void* stream,
+                          const gmm_fp8_tile_config* config) {
+  return fp8_entry(xq, xs, wq4, ws, group_sizes, G, M, K, N, fuse_silu_mul ? 1 : 0, out, nullptr, nullptr, false,
+                   workspace, workspace_bytes, stream, config, 1);
+}
+
+gmm_status gmm_fp8_w4_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq4, const float* ws,
+                                       const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
+                                       void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream,
+                                       const gmm_fp8_tile_config* config) {
+  return fp8_entry(xq, xs, wq4, ws, group_sizes, G, M, K, N, 1, h, hq, hs, true, workspace, workspace_bytes, stream,
+                   config, 1);
 }
 
 gmm_status gmm_bf16_fwd(const void* x, const void* w, const int32_t* group_sizes, int G, int64_t M, int64_t K,

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -69,6 +70,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // the same bits.
 __device__ __forceinline__ void e4m3_block_scale(float absmax, float& s, float& inv) {
   s = __fdiv_rn(absmax, 448.0f);
+  inv = (s == 0.0f) ? 0.0f : __fdiv_rn(1.0f, s);
+}
+// The same block rule for 4-bit E2M1 weight codes, whose largest value is 6
+// ("实现差距：GMM Kernel（V1 vs V2）", §3.4: 4-bit weight types with the
+// blockwise fp32 scales kept): scale = absmax / 6, inv = (scale == 0 ? 0 :
+// 1 / scale).
+__device__ __forceinline__ void e2m1_block_scale(float absmax, float& s, float& inv) {
+  s = __fdiv_rn(absmax, 6.0f);
   inv = (s == 0.0f) ? 0.0f : __fdiv_rn(1.0f, s);
 }
 // 2 x fp32 -> 2 x e4m3; `lo` is the lower byte.

@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // bytes a stage's copies count on its barrier: 4-bit weights count
+      // their packed size (64 bytes per 128-code row), though they land
+      // expanded to the e4m3 operand's footprint in shared memory
+      const uint32_t stage_tx = C::kABytes + (args.b_fmt != 0 ? C::kBBytes / 2 : C::kBBytes);
       uint32_t c = 0;
       bool ok = true;
       for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* a_dst = ring + s * C::kStageBytes;
           uint8_t* b_dst = a_dst + C::kABytes;
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          mbar_arrive_expect_tx(&full[s], stage_tx);
           tma_load_2d(a_dst, &map_a, &full[s], kb * 128, tl.row0);
           if (FUSE) {
             tma_load_2d(b_dst, &map_b, &full[s], kb * 128, brow);
@@ -192,7 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(0u /*e4m3*/, false, false, kBM, BN);
+      // A e4m3; B e4m3, or e2m1 for 4-bit weights (bits 10-12)
+      const uint32_t idesc =
+          (make_idesc(0u /*e4m3*/, false, false, kBM, BN) & ~(7u << 10)) | (static_cast<uint32_t>(args.b_fmt) << 10);
       uint32_t c = 0, t = 0;
       bool ok = true;
       for (uint32_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {

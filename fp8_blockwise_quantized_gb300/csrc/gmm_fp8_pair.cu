@@ -152,6 +152,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+      // bytes this CTA's copies count per stage (4-bit weights: their packed
+      // size, half of the e4m3 operand's shared-memory footprint)
+      const uint32_t stage_tx = C::kABytes + (args.b_fmt != 0 ? C::kBHalfBytes : 2 * C::kBHalfBytes);
       uint32_t c = 0;
       bool ok = true;
       for (TileWalk w(args.pair_tiles, units_per_tile, num_units, num_tiles, col_major, first, step); w.live() && ok;
@@ -170,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* a_dst = ring + s * C::kStageBytes;
           uint8_t* b_dst = a_dst + C::kABytes;
           if (leader) {
-            mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+            mbar_arrive_expect_tx(&full[s], stage_tx);
             tma_load_2d(a_dst, &map_a, &full[s], kb * 128, arow);
             tma_load_2d(b_dst, &map_b, &full[s], kb * 128, b0);
             tma_load_2d(b_dst + C::kBHalfBytes, &map_b, &full[s], kb * 128, b1);
@@ -179,7 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // the expectation is registered (the count dips below zero
             // within the phase)
             const uint32_t bar = full0 + s * 8u;
-            mbar_arrive_expect_tx_remote(bar, C::kStageBytes);
+            mbar_arrive_expect_tx_remote(bar, stage_tx);
             tma_load_2d_pair(a_dst, &map_a, bar, kb * 128, arow);
             tma_load_2d_pair(b_dst, &map_b, bar, kb * 128, b0);
             tma_load_2d_pair(b_dst + C::kBHalfBytes, &map_b, bar, kb * 128, b1);
@@ -200,7 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
-      constexpr uint32_t idesc = make_idesc(0u /*e4m3*/, false, false, 2 * kBM, kHalfCols);
+      // A e4m3; B e4m3, or e2m1 for 4-bit weights (bits 10-12)
+      const uint32_t idesc = (make_idesc(0u /*e4m3*/, false, false, 2 * kBM, kHalfCols) & ~(7u << 10)) |
+                             (static_cast<uint32_t>(args.b_fmt) << 10);
       uint32_t c = 0, t = 0;
       bool ok = true;
       for (uint32_t u = first; u < num_units && ok; u += step) {

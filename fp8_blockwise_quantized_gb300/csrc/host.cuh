@@ -30,9 +30,10 @@ gmm_status host_fp8_config(int64_t N, int fuse, const gmm_fp8_tile_config* in, i
 // Encodes the tensor maps and launches the FP8 forward with a resolved
 // configuration, after the caller validated the arguments and, when needed,
 // enqueued the group metadata into `workspace` (M > 0).  out: bf16 [M, N] or
-// NULL (fused cast only); hq/hs: the fused FP8 cast of the output or NULL.
+// NULL (fused cast only); hq/hs: the fused FP8 cast of the output or NULL;
+// w4: the weights are packed 4-bit E2M1 codes instead of e4m3.
 gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, const float* ws, int G, int64_t M,
                            int64_t K, int64_t N, int fuse, void* out, void* hq, float* hs, void* workspace,
-                           const gmm_fp8_tile_config& cfg, cudaStream_t s);
+                           const gmm_fp8_tile_config& cfg, cudaStream_t s, int w4);
 
 }  // namespace gmm

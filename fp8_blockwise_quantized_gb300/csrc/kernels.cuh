@@ -39,6 +39,7 @@ cudaError_t launch_group_metadata(const int32_t* sizes, int G, int M, void* work
 constexpr int kLhsBlocksPerWarp = 8;
 __global__ void quantize_lhs_kernel(const uint4* x, int M, int KB, long long nblocks, uint2* xq, float* xs);
 __global__ void quantize_rhs_kernel(const uint16_t* w, int K, int N, uint8_t* wq, float* ws);
+__global__ void quantize_rhs_w4_kernel(const uint16_t* w, int K, int N, uint8_t* wq4, float* ws);
 
 // ---- grouped GEMMs ------------------------------------------------------------
 // Arguments shared by the grouped forward kernels.
@@ -55,6 +56,8 @@ struct FwdArgs {
   int fuse;               // 1: silu(gate) * up, W has 2N columns
   int bn;                 // FP8: columns of W per unit (0: by N)
   int col_major;          // FP8: units ordered column block major
+  int b_fmt;              // FP8: weight code type in the MMA instruction descriptor
+                          // (kind::f8f6f4: 0 = e4m3, 5 = e2m1)
   uint64_t wait_limit_ns;
 };
 

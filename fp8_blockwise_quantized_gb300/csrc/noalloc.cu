@@ -105,5 +105,5 @@ extern "C" gmm_status gmm_fp8_fwd_noalloc(const void* xq, const float* xs, const
   e = launch_group_metadata(group_sizes, G, static_cast<int>(M), d.scratch, s);
   if (e != cudaSuccess) return host_cuda_fail(e, "group_metadata_kernel launch");
   if (M == 0) return GMM_OK;
-  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, nullptr, nullptr, d.scratch, cfg, s);
+  return host_fp8_launch(xq, xs, wq, ws, G, M, K, N, fuse, out, nullptr, nullptr, d.scratch, cfg, s, 0);
 }

@@ -157,4 +157,64 @@ __global__ void __launch_bounds__(256) quantize_rhs_kernel(const uint16_t* __res
   if (t == 0) ws[(g * KB + kb) * NB + nb] = s;
 }
 
+// RHS, 128x128 blocks, 4-bit E2M1 codes, offline ("实现差距：GMM Kernel（V1 vs
+// V2）", §3.4).  As quantize_rhs_kernel with scale = absmax / 6; the codes go
+// out packed two per byte in the K-major layout [G][N][K/2]: byte k/2 of row
+// n holds the code of k (even) in its low nibble and that of k + 1 in its
+// high nibble, the order in which the tensor core reads 4-bit operands.
+__global__ void __launch_bounds__(256) quantize_rhs_w4_kernel(const uint16_t* __restrict__ w, int K, int N,
+                                                              uint8_t* __restrict__ wq4, float* __restrict__ ws) {
+  __shared__ float red[8];
+  __shared__ uint8_t tile[128][128 + 16];  // [n][k] codes, one per byte, padded
+  const int KB = K / 128, NB = N / 128;
+  const int nb = blockIdx.x % NB;
+  const int kb = (blockIdx.x / NB) % KB;
+  const long long g = blockIdx.x / (static_cast<long long>(NB) * KB);
+  const int t = threadIdx.x;
+  const int kr = t >> 1, c0 = (t & 1) * 64;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      w + (g * K + static_cast<long long>(kb) * 128 + kr) * N + static_cast<long long>(nb) * 128 + c0);
+  float f[64];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float e[8];
+    bf16x8_to_f32(src[i], e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[8 * i + j] = e[j];
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  if ((t & 31) == 0) red[t >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  float s, inv;
+  e2m1_block_scale(amax, s, inv);
+#pragma unroll
+  for (int j = 0; j < 64; ++j)
+    tile[c0 + j][kr] =
+        static_cast<uint8_t>(__nv_cvt_float_to_fp4(__fmul_rn(f[j], inv), __NV_E2M1, cudaRoundNearest) & 0xF);
+  __syncthreads();
+  // write out: thread t -> output row n = t/2 of the block, 64 codes = 32 bytes
+  const int nr = t >> 1, k0 = (t & 1) * 64;
+  uint8_t* dst = wq4 + (g * N + static_cast<long long>(nb) * 128 + nr) * (K / 2) + static_cast<long long>(kb) * 64 +
+                 k0 / 2;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t word[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint8_t* p = &tile[nr][k0 + 32 * i + 8 * q];
+      word[q] = static_cast<uint32_t>(p[0] | (p[1] << 4)) | (static_cast<uint32_t>(p[2] | (p[3] << 4)) << 8) |
+                (static_cast<uint32_t>(p[4] | (p[5] << 4)) << 16) | (static_cast<uint32_t>(p[6] | (p[7] << 4)) << 24);
+    }
+    reinterpret_cast<uint4*>(dst)[i] = make_uint4(word[0], word[1], word[2], word[3]);
+  }
+  if (t == 0) ws[(g * KB + kb) * NB + nb] = s;
+}
+
 }  // namespace gmm

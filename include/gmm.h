@@ -218,6 +218,42 @@ gmm_status gmm_fp8_fwd_swiglu_quant_tiled(const void* xq, const float* xs, const
                                           void* stream, const gmm_fp8_tile_config* config);
 
 /*
+ * Sub-byte weights ("实现差距：GMM Kernel（V1 vs V2）", §3.4: the V2 kernel
+ * takes int4 / float4_e2m1fn weight tiles and keeps the blockwise fp32-scale
+ * arithmetic; §4.1 lists MXFP4 weights as the missing piece).  Here: FP4 E2M1
+ * weight codes (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; values
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives) with one fp32 scale per
+ * 128x128 block, scale = absmax / 6 (the same rule as gmm_quantize_rhs with
+ * 6, the largest E2M1 value, in place of 448), codes = e2m1(w * (1/scale)),
+ * nearest even, saturating at 6.  The weights stay packed (half the bytes of
+ * e4m3) until the copy into shared memory expands them for the tensor core.
+ *   w    bf16 [G, K, N]
+ *   wq4  packed codes [G, N, K/2] bytes (K-major): byte (g*N + n)*K/2 + k/2
+ *        holds the code of w[g][k][n] for even k in its low 4 bits and that
+ *        of k + 1 in its high 4 bits; 32-byte aligned
+ *   ws   fp32 [G, K/128, N/128]
+ */
+gmm_status gmm_quantize_rhs_w4(const void* w, int G, int64_t K, int64_t N, void* wq4, float* ws, void* stream);
+
+/*
+ * The FP8 forward (gmm_fp8_fwd_tiled, gmm_fp8_fwd_swiglu_quant_tiled) with
+ * 4-bit weights: the activations are e4m3 in 1x128 blocks as before, the
+ * weights E2M1 codes as written by gmm_quantize_rhs_w4 (wq4 32-byte aligned),
+ * each 128-wide K block's partial P_kb = sum_k xq[m,k] * wq4[g,k,n] formed on
+ * the tensor core (e4m3 x e2m1, fp32) and promoted with xs[kb,m] *
+ * ws[g,kb,n/128] exactly as for e4m3 weights.  Same arguments, layouts,
+ * tile configurations (config may be NULL) and errors otherwise.
+ */
+gmm_status gmm_fp8_w4_fwd(const void* xq, const float* xs, const void* wq4, const float* ws,
+                          const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, int fuse_silu_mul,
+                          void* out, void* workspace, size_t workspace_bytes, void* stream,
+                          const gmm_fp8_tile_config* config);
+gmm_status gmm_fp8_w4_fwd_swiglu_quant(const void* xq, const float* xs, const void* wq4, const float* ws,
+                                       const int32_t* group_sizes, int G, int64_t M, int64_t K, int64_t N, void* h,
+                                       void* hq, float* hs, void* workspace, size_t workspace_bytes, void* stream,
+                                       const gmm_fp8_tile_config* config);
+
+/*
  * a7 — bf16 GMM forward, unquantized (the BF16 baseline of "GEMM Kernel
  * 性能优化十问", Q7/Q10 step 4): out[m,n] = bf16(sum_k x[m,k] * w[g,k,n]),
  * fp32 accumulation; fuse_silu_mul as for gmm_fp8_fwd.
