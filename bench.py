@@ -15,6 +15,10 @@ TFLOP/s counted as 2*M*K*N per GMM (FLOPs do not depend on precision, Q7),
 summed over the four GMMs.  Weights are quantized once, offline, before
 timing (128x128 blocks, as the method prescribes for static weights).
 
+Beside the step (not in it) the same FP8 forward launches run with 4-bit E2M1
+weights (packed two codes per byte, 128x128 fp32 scales), the bf16 forward of
+both layers and the layer's bf16 dgrad.
+
 Inputs are synthetic and seeded: routing from Zipf(1.1) expert popularity
 with 8 dead experts, X ~ N(0,1) with 1% x50 outliers, W ~ N(0, 1/K), upstream
 gradients ~ N(0,1).  Inputs are resident in HBM before the timed region;
@@ -423,6 +427,46 @@ def run_gpu(args):
                                          ((dh_ms + dx_ms) * 1e-3) / 1e12 / bf_peak, 3),
                  "note": "bf16 dgrad of the layer (dY . W_wo^T, d(gate|up) . W_wi^T), timed beside the step"}
 
+    # ---------------- 4-bit (E2M1) weights, timed beside the step (not in it):
+    # the same fused wi (writing h and its FP8 cast) and wo with the weights
+    # packed two codes per byte, against the e4m3 launches of the step
+    w4 = None
+    if not args.no_w4:
+        wq4_wi, ws4_wi = gmm.quantize_rhs_w4(w_wi)   # offline, untimed
+        wq4_wo, ws4_wo = gmm.quantize_rhs_w4(w_wo)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        chk(gmm.gmm_group_metadata(sizes, G, M, work.buf, work.nbytes, stream), "metadata")
+        t4 = []
+        for i in range(max(3, min(args.steps, 100))):
+            flush.zero_()
+            ev[0].record(stream)
+            chk(gmm.gmm_fp8_w4_fwd_swiglu_quant(xq, xs, wq4_wi, ws4_wi, None, G, M, K, N, h, hq, hs, work.buf,
+                                                work.nbytes, stream), "w4 wi")
+            ev[1].record(stream)
+            chk(gmm.gmm_fp8_w4_fwd(hq, hs, wq4_wo, ws4_wo, None, G, M, N, K, 0, y, work.buf, work.nbytes, stream),
+                "w4 wo")
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 1:
+                t4.append((ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])))
+        st4 = work.status(stream)
+        if st4 != 0:
+            raise RuntimeError(f"device status {gmm.STATUS_NAMES.get(st4, st4)} after the 4-bit weight runs")
+        live = int(np.count_nonzero(sizes_np))
+        w4_bytes = {"wi": nbytes["gmm_fp8_wi"] - live * K * 2 * N // 2,
+                    "wo": nbytes["gmm_fp8_wo"] - live * N * K // 2}
+        w4 = {}
+        for j, nm in enumerate(("wi", "wo")):
+            ms4 = float(np.mean([t[j] for t in t4]))
+            ref = kern[f"gmm_fp8_{nm}"]
+            w4[nm] = {"ms": round(ms4, 4), "bytes": w4_bytes[nm],
+                      "GB/s": round(w4_bytes[nm] / (ms4 * 1e-3) / 1e9, 1),
+                      "TFLOP/s": round(flops[f"gmm_fp8_{nm}"] / (ms4 * 1e-3) / 1e12, 1),
+                      "e4m3_ms": ref["ms"], "e4m3_bytes": ref["bytes"],
+                      "speedup_over_e4m3": round(ref["ms"] / ms4, 3)}
+        w4["note"] = ("E2M1 weights, 128x128 fp32 scales, packed two codes per byte in HBM; the live experts' "
+                      "weight read halves; timed beside the step (the step itself uses e4m3 weights)")
+
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.no_e2e:
@@ -529,7 +573,7 @@ def run_gpu(args):
         "roofline": roof, "kernels": kern,
         "kernels_note": f"per-kernel times from a second pass of {n_split} steps with an event between every "
                         "call (the timed steps carry boundary events only)",
-        "bf16_fwd_baseline": bf or None, "bf16_dgrad": dgrad, "e2e": e2e,
+        "bf16_fwd_baseline": bf or None, "bf16_dgrad": dgrad, "w4_weights": w4, "e2e": e2e,
         "cpu_baseline": cpu, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
     }
@@ -696,7 +740,20 @@ def run_profile_case(args):
     def bf16(shape, std=1.0):
         return (torch.randn(shape, generator=gen, device=dev) * std).to(torch.bfloat16)
 
-    if case in ("fp8_wi", "fp8_wo", "fp8_wi_quant"):
+    if case == "fp8_w4_wi_quant":
+        x = bf16((M, K))
+        xq, xs = gmm.quantize_lhs(x)
+        w = bf16((G, K, 2 * N), 1.0 / math.sqrt(K))
+        wq, ws = gmm.quantize_rhs_w4(w)
+        del x, w
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        hq = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        hs = torch.empty((N // 128, M), dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        run = lambda: chk(gmm.gmm_fp8_w4_fwd_swiglu_quant(xq, xs, wq, ws, sizes, G, M, K, N, out, hq, hs, work.buf,
+                                                          work.nbytes, None), case)
+    elif case in ("fp8_wi", "fp8_wo", "fp8_wi_quant"):
         k, n, fuse = (K, N, 1) if case != "fp8_wo" else (N, K, 0)
         x = bf16((M, k))
         xq, xs = gmm.quantize_lhs(x)
@@ -746,8 +803,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-bf16-baseline", action="store_true")
+    ap.add_argument("--no-w4", action="store_true", help="skip the 4-bit weight forward timed beside the step")
     ap.add_argument("--profile-case", default=None,
-                    choices=["fp8_wi", "fp8_wi_quant", "fp8_wo", "tgmm_wi", "tgmm_wo", "quantize_x"],
+                    choices=["fp8_wi", "fp8_wi_quant", "fp8_w4_wi_quant", "fp8_wo", "tgmm_wi", "tgmm_wo",
+                             "quantize_x"],
                     help="run one kernel at the production shape (for ncu) and exit")
     ap.add_argument("--oracle-configs", action="store_true",
                     help="time the CPU oracle on the four small configurations (all cores and one core) and exit")
