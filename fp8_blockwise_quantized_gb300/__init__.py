@@ -13,7 +13,7 @@ from .binding import (EXPORTED, GmmError, LIB_PATH, STATUS_NAMES, Workspace, bf1
                       gmm_quantize_lhs, gmm_quantize_rhs, gmm_tiles_offset, gmm_workspace_bytes,
                       group_metadata, load, quantize_lhs, quantize_rhs, tgmm, tgmm_bf16,
                       gmm_quantize_rhs_w4, gmm_fp8_w4_fwd, gmm_fp8_w4_fwd_swiglu_quant, quantize_rhs_w4,
-                      fp8_w4_fwd, fp8_w4_fwd_swiglu_quant)
+                      fp8_w4_fwd, fp8_w4_fwd_swiglu_quant, tgmm_bf16_tiled, TgmmConfig)
 
 __all__ = ["EXPORTED", "GmmError", "LIB_PATH", "STATUS_NAMES", "Workspace", "bf16_fwd", "dgrad", "fp8_fwd",
            "gmm_bf16_dgrad", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_swiglu_quant", "fp8_fwd_swiglu_quant",
@@ -23,4 +23,4 @@ __all__ = ["EXPORTED", "GmmError", "LIB_PATH", "STATUS_NAMES", "Workspace", "bf1
            "gmm_quantize_lhs", "gmm_quantize_rhs", "gmm_tiles_offset", "gmm_workspace_bytes",
            "group_metadata", "load", "quantize_lhs", "quantize_rhs", "tgmm", "tgmm_bf16",
            "gmm_quantize_rhs_w4", "gmm_fp8_w4_fwd", "gmm_fp8_w4_fwd_swiglu_quant", "quantize_rhs_w4",
-           "fp8_w4_fwd", "fp8_w4_fwd_swiglu_quant"]
+           "fp8_w4_fwd", "fp8_w4_fwd_swiglu_quant", "tgmm_bf16_tiled", "TgmmConfig"]

@@ -31,19 +31,29 @@ EXPORTED = ["gmm_status_string", "gmm_last_cuda_error", "gmm_workspace_bytes", "
             "gmm_bf16_fwd", "tgmm_bf16", "gmm_get_device_status", "gmm_fp8_fwd_noalloc",
             "gmm_bf16_dgrad", "gmm_fp8_fwd_swiglu_quant", "gmm_selftest_wait_timeout", "gmm_fp8_fwd_tiled",
             "gmm_fp8_fwd_swiglu_quant_tiled", "gmm_quantize_rhs_w4", "gmm_fp8_w4_fwd",
-            "gmm_fp8_w4_fwd_swiglu_quant"]
+            "gmm_fp8_w4_fwd_swiglu_quant", "tgmm_bf16_tiled"]
 
 
 class TileConfig(ctypes.Structure):
     """gmm_fp8_tile_config: bn (128 | 256), ctas (1 .. SMs), unit_order
     (1 row-tile major, 2 column-block major), cta_group (1 one CTA per
-    128-row tile, 2 CTA pairs on 256-row tiles); 0 keeps a field's default.
+    128-row tile, 2 CTA pairs on 256-row tiles), stages (operand ring
+    slots), tmem_bufs (TMEM partial buffers); 0 keeps a field's default.
     A shorter tuple leaves the remaining fields 0."""
     _fields_ = [("bn", ctypes.c_int), ("ctas", ctypes.c_int), ("unit_order", ctypes.c_int),
-                ("cta_group", ctypes.c_int)]
+                ("cta_group", ctypes.c_int), ("stages", ctypes.c_int), ("tmem_bufs", ctypes.c_int)]
 
     def astuple(self):
-        return (self.bn, self.ctas, self.unit_order, self.cta_group)
+        return (self.bn, self.ctas, self.unit_order, self.cta_group, self.stages, self.tmem_bufs)
+
+
+class TgmmConfig(ctypes.Structure):
+    """gmm_tgmm_tile_config: stages (4..6), claim_ahead (1..12), max_batch
+    (1..4); 0 keeps a field's default.  A shorter tuple leaves the rest 0."""
+    _fields_ = [("stages", ctypes.c_int), ("claim_ahead", ctypes.c_int), ("max_batch", ctypes.c_int)]
+
+    def astuple(self):
+        return (self.stages, self.claim_ahead, self.max_batch)
 
 
 class GmmError(RuntimeError):
@@ -92,6 +102,8 @@ def load():
     lib.gmm_bf16_fwd.argtypes = [P, P, P, I, I64, I64, I64, I, P, P, SZ, P]
     lib.tgmm_bf16.restype = I
     lib.tgmm_bf16.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P]
+    lib.tgmm_bf16_tiled.restype = I
+    lib.tgmm_bf16_tiled.argtypes = [P, P, P, I, I64, I64, I64, P, P, SZ, P, ctypes.POINTER(TgmmConfig)]
     lib.gmm_fp8_fwd_swiglu_quant.restype = I
     lib.gmm_fp8_fwd_swiglu_quant.argtypes = [P, P, P, P, P, I, I64, I64, I64, P, P, P, P, SZ, P]
     lib.gmm_fp8_fwd_swiglu_quant_tiled.restype = I
@@ -169,7 +181,7 @@ def gmm_fp8_fwd(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, wor
 
 def gmm_fp8_fwd_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, fuse_silu_mul, out, workspace,
                       workspace_bytes, stream=None, config=None) -> int:
-    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group]) tuple, or None (defaults)."""
+    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group[, stages[, tmem_bufs]]]) tuple, or None."""
     if config is not None and not isinstance(config, TileConfig):
         config = TileConfig(*config)
     return load().gmm_fp8_fwd_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
@@ -185,7 +197,7 @@ def gmm_fp8_fwd_swiglu_quant(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs,
 
 def gmm_fp8_fwd_swiglu_quant_tiled(xq, xs, wq, ws, group_sizes, G, M, K, N, h, hq, hs, workspace,
                                    workspace_bytes, stream=None, config=None) -> int:
-    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group]) tuple, or None (defaults)."""
+    """config: a TileConfig, a (bn, ctas, unit_order[, cta_group[, stages[, tmem_bufs]]]) tuple, or None."""
     if config is not None and not isinstance(config, TileConfig):
         config = TileConfig(*config)
     return load().gmm_fp8_fwd_swiglu_quant_tiled(_p(xq), _p(xs), _p(wq), _p(ws), _p(group_sizes), G, M, K, N,
@@ -232,6 +244,15 @@ def gmm_bf16_dgrad(dy, w, group_sizes, G, M, K, N, dx, workspace, workspace_byte
 def tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, stream=None) -> int:
     return load().tgmm_bf16(_p(x), _p(dy), _p(group_sizes), G, M, K, N, _p(dw), _p(workspace),
                             workspace_bytes, _s(stream))
+
+
+def tgmm_bf16_tiled(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, stream=None,
+                    config=None) -> int:
+    """config: a TgmmConfig, a (stages, claim_ahead, max_batch) tuple, or None (defaults)."""
+    if config is not None and not isinstance(config, TgmmConfig):
+        config = TgmmConfig(*config)
+    return load().tgmm_bf16_tiled(_p(x), _p(dy), _p(group_sizes), G, M, K, N, _p(dw), _p(workspace),
+                                  workspace_bytes, _s(stream), ctypes.byref(config) if config is not None else None)
 
 
 def gmm_get_device_status(workspace, stream=None) -> int:
@@ -438,7 +459,7 @@ def dgrad(dy, w, group_sizes, dx=None, workspace=None, stream=None):
     return dx
 
 
-def tgmm(x, dy, group_sizes, dw=None, workspace=None, stream=None):
+def tgmm(x, dy, group_sizes, dw=None, workspace=None, stream=None, config=None):
     M, K = x.shape
     M2, N = dy.shape
     assert M2 == M
@@ -453,7 +474,11 @@ def tgmm(x, dy, group_sizes, dw=None, workspace=None, stream=None):
     if dw is None:
         dw = torch.empty((G, K, N), dtype=torch.bfloat16, device=x.device)
     ws_ = _ws_for(group_sizes, workspace, G, M, x.device)
-    _check(tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, ws_.buf, ws_.nbytes, stream), "tgmm_bf16")
+    if config is None:
+        _check(tgmm_bf16(x, dy, group_sizes, G, M, K, N, dw, ws_.buf, ws_.nbytes, stream), "tgmm_bf16")
+    else:
+        _check(tgmm_bf16_tiled(x, dy, group_sizes, G, M, K, N, dw, ws_.buf, ws_.nbytes, stream, config),
+               "tgmm_bf16_tiled")
     return dw
 
 

@@ -199,7 +199,7 @@ int host_fp8_default_cta_group(int64_t, int, int, int) {
 }
 
 gmm_status host_fp8_config(int64_t N, int fuse, const gmm_fp8_tile_config* in, int sms, gmm_fp8_tile_config* out) {
-  gmm_fp8_tile_config c = in ? *in : gmm_fp8_tile_config{0, 0, 0, 0};
+  gmm_fp8_tile_config c = in ? *in : gmm_fp8_tile_config{0, 0, 0, 0, 0, 0};
   if (c.cta_group == 0) c.cta_group = host_fp8_default_cta_group(N, fuse, c.bn, c.ctas);
   if (c.cta_group != 1 && c.cta_group != 2) return GMM_ERR_UNSUPPORTED;
   if (c.bn != 0 && c.bn != 128 && c.bn != 256) return GMM_ERR_UNSUPPORTED;
@@ -217,6 +217,23 @@ gmm_status host_fp8_config(int64_t N, int fuse, const gmm_fp8_tile_config* in, i
   }
   if (c.ctas == 0) c.ctas = c.cta_group == 2 ? sms - sms % 2 : sms;
   if (c.unit_order == 0) c.unit_order = 1;
+  // compiled instances: ring slots and TMEM partial buffers
+  int smin, smax, sdef, bdef;
+  bool bufs_ok;
+  if (c.cta_group == 2) {
+    smin = 3, smax = fuse ? 5 : 4, sdef = smax, bdef = 4;
+    bufs_ok = c.tmem_bufs == 0 || c.tmem_bufs == 4;
+  } else if (c.bn == 256) {
+    smin = 2, smax = 3, sdef = 3, bdef = 2;
+    bufs_ok = c.tmem_bufs == 0 || c.tmem_bufs == 2;
+  } else {
+    smin = 3, smax = 5, sdef = 4, bdef = 2;
+    bufs_ok = c.tmem_bufs == 0 || c.tmem_bufs == 2 || c.tmem_bufs == 4;
+  }
+  if (c.stages != 0 && (c.stages < smin || c.stages > smax)) return GMM_ERR_UNSUPPORTED;
+  if (!bufs_ok) return GMM_ERR_UNSUPPORTED;
+  if (c.stages == 0) c.stages = sdef;
+  if (c.tmem_bufs == 0) c.tmem_bufs = bdef;
   *out = c;
   return GMM_OK;
 }
@@ -262,6 +279,8 @@ gmm_status host_fp8_launch(const void* xq, const float* xs, const void* wq, cons
   a.bn = geo.bn_mma;
   a.col_major = cfg.unit_order == 2 ? 1 : 0;
   a.b_fmt = w4 ? 5 : 0;  // kind::f8f6f4 operand types: e2m1 or e4m3
+  a.stages = cfg.stages;
+  a.tmem_bufs = cfg.tmem_bufs;
   a.wait_limit_ns = host_wait_limit_ns();
   const long long tiles = pair ? pair_tiles_capacity(G, M) : tiles_capacity(G, M);
   const long long max_units = tiles * (N / geo.out_cols);
@@ -518,8 +537,21 @@ gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_si
 
 gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M, int64_t K,
                      int64_t N, void* dw, void* workspace, size_t workspace_bytes, void* stream) {
+  return tgmm_bf16_tiled(x, dy, group_sizes, G, M, K, N, dw, workspace, workspace_bytes, stream, nullptr);
+}
+
+gmm_status tgmm_bf16_tiled(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M, int64_t K,
+                           int64_t N, void* dw, void* workspace, size_t workspace_bytes, void* stream,
+                           const gmm_tgmm_tile_config* config) {
   gmm_status st = check_grouped(G, M, K, N, N);
   if (st != GMM_OK) return st;
+  gmm_tgmm_tile_config cfg = config ? *config : gmm_tgmm_tile_config{0, 0, 0};
+  if (cfg.stages != 0 && (cfg.stages < 4 || cfg.stages > 6)) return GMM_ERR_UNSUPPORTED;
+  if (cfg.claim_ahead < 0 || cfg.claim_ahead > 12 || cfg.max_batch < 0 || cfg.max_batch > 4)
+    return GMM_ERR_UNSUPPORTED;
+  if (cfg.stages == 0) cfg.stages = 6;
+  if (cfg.claim_ahead == 0) cfg.claim_ahead = 3;
+  if (cfg.max_batch == 0) cfg.max_batch = 4;
   // the kernel walks its output tiles with 32-bit indices
   if (static_cast<int64_t>(G) * (K / 128) * (N / tgmm_bn(static_cast<int>(N))) > INT32_MAX / 2) return GMM_ERR_SHAPE;
   if (!dw) return GMM_ERR_NULL;
@@ -550,6 +582,9 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
   a.M = static_cast<int>(M);
   a.K = static_cast<int>(K);
   a.N = static_cast<int>(N);
+  a.stages = cfg.stages;
+  a.claim_ahead = cfg.claim_ahead;
+  a.max_batch = cfg.max_batch;
   a.wait_limit_ns = wait_limit_ns();
   const long long units = static_cast<long long>(G) * (K / 128) * (N / tgmm_bn(static_cast<int>(N)));
   const int grid = static_cast<int>(units < di.sms ? units : di.sms);

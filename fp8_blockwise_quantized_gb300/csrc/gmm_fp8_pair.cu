@@ -60,11 +60,11 @@ constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad
 constexpr int kTBufs = 4;              // TMEM buffers of one half (128 columns) each
 constexpr int kHalfCols = 128;
 
-template <bool FUSE>
+template <bool FUSE, int STAGES>
 struct PairTile {
   static constexpr int kBoxes = FUSE ? 1 : 2;  // 32x64 bf16 staging boxes per promotion warp
   static constexpr int kStagingBytes = kPromoWarps * kBoxes * 4096;
-  static constexpr int kStages = FUSE ? 5 : 4;
+  static constexpr int kStages = STAGES;       // ring slots (default 5 fused, 4 otherwise)
   static constexpr int kABytes = kBM * 128;        // this CTA's 128 rows x 128 K bytes
   static constexpr int kBHalfBytes = 64 * 128;     // this CTA's 64 columns of a half
   static constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
@@ -73,14 +73,15 @@ struct PairTile {
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kBarBytes;
   static_assert(8 * (2 * kStages + 2 * kTBufs + 2 * kScaleSlots + 3) + 8 <= kBarBytes, "barrier area");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
-template <bool FUSE, bool QUANT>
+template <bool FUSE, bool QUANT, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gmm_fp8_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_out, const FwdArgs args) {
   static_assert(!QUANT || FUSE, "the quantized output is for the fused units");
-  using C = PairTile<FUSE>;
+  using C = PairTile<FUSE, STAGES>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -495,12 +496,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
 }
 
-template <bool FUSE, bool QUANT>
+template <bool FUSE, bool QUANT, int STAGES>
 cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                    const FwdArgs& args, int max_pairs, cudaStream_t stream) {
-  constexpr int smem = PairTile<FUSE>::kSmemBytes;
-  cudaError_t e =
-      cudaFuncSetAttribute(gmm_fp8_pair_kernel<FUSE, QUANT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = PairTile<FUSE, STAGES>::kSmemBytes;
+  auto kernel = gmm_fp8_pair_kernel<FUSE, QUANT, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // as many pairs as can be resident at once (one CTA per SM)
   cudaLaunchConfig_t cfg = {};
@@ -509,21 +510,30 @@ cudaError_t launch(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUt
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, gmm_fp8_pair_kernel<FUSE, QUANT>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const int pairs = clusters < max_pairs ? clusters : max_pairs;
-  return launch_pdl(gmm_fp8_pair_kernel<FUSE, QUANT>, dim3(2 * pairs), dim3(kThreads), smem, stream, map_a, map_b,
-                    map_out, args);
+  return launch_pdl(kernel, dim3(2 * pairs), dim3(kThreads), smem, stream, map_a, map_b, map_out, args);
+}
+
+template <bool FUSE, bool QUANT>
+cudaError_t launch_stages(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                          const FwdArgs& args, int max_pairs, cudaStream_t stream) {
+  if (args.stages == 3) return launch<FUSE, QUANT, 3>(map_a, map_b, map_out, args, max_pairs, stream);
+  if constexpr (FUSE) {
+    if (args.stages != 4) return launch<FUSE, QUANT, 5>(map_a, map_b, map_out, args, max_pairs, stream);
+  }
+  return launch<FUSE, QUANT, 4>(map_a, map_b, map_out, args, max_pairs, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_gmm_fp8_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                                 const FwdArgs& args, int max_pairs, cudaStream_t stream) {
-  if (args.fuse && args.hq) return launch<true, true>(map_a, map_b, map_out, args, max_pairs, stream);
-  if (args.fuse) return launch<true, false>(map_a, map_b, map_out, args, max_pairs, stream);
-  return launch<false, false>(map_a, map_b, map_out, args, max_pairs, stream);
+  if (args.fuse && args.hq) return launch_stages<true, true>(map_a, map_b, map_out, args, max_pairs, stream);
+  if (args.fuse) return launch_stages<true, false>(map_a, map_b, map_out, args, max_pairs, stream);
+  return launch_stages<false, false>(map_a, map_b, map_out, args, max_pairs, stream);
 }
 
 }  // namespace gmm

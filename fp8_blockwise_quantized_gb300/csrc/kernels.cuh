@@ -58,6 +58,8 @@ struct FwdArgs {
   int col_major;          // FP8: units ordered column block major
   int b_fmt;              // FP8: weight code type in the MMA instruction descriptor
                           // (kind::f8f6f4: 0 = e4m3, 5 = e2m1)
+  int stages;             // FP8: ring slots of the launched instance
+  int tmem_bufs;          // FP8: TMEM partial buffers of the launched instance
   uint64_t wait_limit_ns;
 };
 
@@ -66,6 +68,9 @@ struct TgmmArgs {
   const int32_t* order;   // workspace: groups by size, descending
   uint16_t* dw;           // bf16 [G][K][N]
   int G, M, K, N;
+  int stages;             // CTA-pair kernel with 256-column units: ring slots (4..6)
+  int claim_ahead;        // CTA-pair kernel: units claimed beyond the producer (1..12)
+  int max_batch;          // CTA-pair kernel: most small units per claim (1..4)
   uint64_t wait_limit_ns;
 };
 
@@ -74,6 +79,9 @@ struct TgmmArgs {
 // 32 rows, 128-byte swizzle; read only when args.out is not null.
 cudaError_t launch_gmm_fp8(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
                            const FwdArgs& args, int grid, cudaStream_t stream);
+// The single-CTA kernel's BN = 128 instances (gmm_fp8_n128.cu).
+cudaError_t launch_gmm_fp8_n128(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,
+                                const FwdArgs& args, int grid, cudaStream_t stream);
 // The CTA-pair FP8 kernel: map_b's box is 64 rows (half of a 128-column MMA
 // half); at most max_pairs clusters of two CTAs.
 cudaError_t launch_gmm_fp8_pair(const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_out,

@@ -346,12 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // barrier, in the odd CTA's.  Every role of both CTAs takes the units from
 // its queue in the same order and frees an entry on the even CTA once it has
 // read it.  The last CTA to finish resets the counters for the next launch.
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 6;  // default ring slots with BN = 256 (4 or 5 selectable)
 constexpr int kPairThreads = 352;
 constexpr int kSchedWarp = 10;
 constexpr int kQueue = 16;
 constexpr int kQueueReaders = 2 * (2 + kEpiWarps);  // producer, warp 1, epilogue warps; both CTAs
-constexpr int kClaimAhead = 3;  // units claimed beyond those the even CTA's producer has taken
+// the scheduler claims at most TgmmArgs::claim_ahead units (default 3) beyond
+// those the even CTA's producer has taken, and up to TgmmArgs::max_batch
+// (1..kMaxBatch, default 4) small units per claim
 
 // Zero rows [from, to) of both 64-row x boxes of a ring slot (128 bytes per
 // row and box, so the swizzle does not matter) and fence them into the async
@@ -366,19 +368,20 @@ __device__ __forceinline__ void zero_x_rows(uint8_t* a_ptr, int from, int to, in
   fence_proxy_async_smem();
 }
 
-template <int BN>
+template <int BN, int STAGES>
 struct TgmmPairTile {
   static constexpr int kBoxBytes = kChunk * 64 * 2;           // 64 rows x 64 bf16 = 8 KB
   static constexpr int kABytes = 2 * kBoxBytes;               // this CTA's 128 k columns
   static constexpr int kBBytes = (BN / 2 / 64) * kBoxBytes;   // this CTA's BN/2 n columns
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = BN == 256 ? kPairStages : 8;
+  static constexpr int kStages = STAGES;  // kPairStages (or 4, 5) with BN = 256; 8 with BN = 128
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kStagingBytes = kEpiWarps * 4096;
   // queue entries (16 bytes each), then the barriers, the TMEM address and the abort word
   static constexpr int kTailBytes = 16 * kQueue + 8 * (3 * kStages + 5 + 2 * kQueue) + 12;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 1024;
   static_assert(kTailBytes <= 1024, "barrier area");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Entry i of a CTA's unit queue (every lane of the calling warp, or the one
@@ -408,11 +411,11 @@ struct UnitQueue {
   }
 };
 
-template <int BN>
+template <int BN, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     tgmm_pair_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_dy,
                      const __grid_constant__ CUtensorMap map_dw, const TgmmArgs args) {
-  using C = TgmmPairTile<BN>;
+  using C = TgmmPairTile<BN, STAGES>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -668,10 +671,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint32_t i = 0;
     auto publish = [&](int4 v) -> bool {
       const uint32_t slot = i % kQueue, ph = (i / kQueue) & 1u;
-      // no more than kClaimAhead entries beyond the producer (bounded wait)
-      if (*taken + kClaimAhead <= static_cast<int>(i)) {
+      // no more than claim_ahead entries beyond the producer (bounded wait)
+      if (*taken + args.claim_ahead <= static_cast<int>(i)) {
         const uint64_t t0 = global_timer_ns();
-        while (*taken + kClaimAhead <= static_cast<int>(i)) {
+        while (*taken + args.claim_ahead <= static_cast<int>(i)) {
           if (*abort_word) return false;
           if (global_timer_ns() - t0 > lim) {
             *abort_word = 1;
@@ -710,7 +713,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         if (ok && j < cnt) ok = publish(make_int4(g[j], (k0 + j) % KPNT, r0[j], r1[j]));
       // the units come largest first: claim more at once as they get small
       const int chunks = (r1[cnt - 1] - r0[cnt - 1] + kChunk - 1) / kChunk;
-      next_batch = chunks >= 4 ? 1 : chunks >= 2 ? 2 : kMaxBatch;
+      next_batch = chunks >= 4 ? 1 : chunks >= 2 ? min(2, args.max_batch) : args.max_batch;
     }
     if (ok) publish(make_int4(-1, 0, 0, 0));
   }
@@ -736,11 +739,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   }
 }
 
-template <int BN>
+template <int BN, int STAGES>
 cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, const CUtensorMap& map_dw,
                         const TgmmArgs& args, int max_pairs, cudaStream_t stream) {
-  constexpr int smem = TgmmPairTile<BN>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(tgmm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = TgmmPairTile<BN, STAGES>::kSmemBytes;
+  auto kernel = tgmm_pair_kernel<BN, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // as many pairs as can be resident at once (one CTA per SM)
   cudaLaunchConfig_t cfg = {};
@@ -749,12 +753,11 @@ cudaError_t launch_pair(const CUtensorMap& map_x, const CUtensorMap& map_dy, con
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, tgmm_pair_kernel<BN>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const int pairs = clusters < max_pairs ? clusters : max_pairs;
-  return launch_pdl(tgmm_pair_kernel<BN>, dim3(2 * pairs), dim3(kPairThreads), smem, stream, map_x, map_dy, map_dw,
-                    args);
+  return launch_pdl(kernel, dim3(2 * pairs), dim3(kPairThreads), smem, stream, map_x, map_dy, map_dw, args);
 }
 
 template <int BN>
@@ -777,8 +780,12 @@ cudaError_t launch_tgmm_bf16(const CUtensorMap& map_x, const CUtensorMap& map_dy
   if (args.K % 256 == 0) {
     // CTA pairs: grid / 2 pairs at most (grid = min(SMs, tiles))
     const int max_pairs = grid / 2 > 0 ? grid / 2 : 1;
-    if (args.N % 256 == 0) return launch_pair<256>(map_x, map_dy, map_dw, args, max_pairs, stream);
-    return launch_pair<128>(map_x, map_dy, map_dw, args, max_pairs, stream);
+    if (args.N % 256 == 0) {
+      if (args.stages == 4) return launch_pair<256, 4>(map_x, map_dy, map_dw, args, max_pairs, stream);
+      if (args.stages == 5) return launch_pair<256, 5>(map_x, map_dy, map_dw, args, max_pairs, stream);
+      return launch_pair<256, kPairStages>(map_x, map_dy, map_dw, args, max_pairs, stream);
+    }
+    return launch_pair<128, 8>(map_x, map_dy, map_dw, args, max_pairs, stream);
   }
   if (args.N % 256 == 0) return launch<256>(map_x, map_dy, map_dw, args, grid, stream);
   return launch<128>(map_x, map_dy, map_dw, args, grid, stream);

@@ -1,23 +1,33 @@
-"""Tile autotuner for the FP8 forward.
+"""Tile autotuner for the FP8 forward and for tgmm.
 
-The search follows "GEMM Kernel 性能优化十问", Q8 and Q9.4.  Tile sizes are
-chosen by a search over candidates measured on the real shapes. A candidate
-may win only after an accuracy check, which a caller can loosen but never
-switch off.
+The search follows "GEMM Kernel 性能优化十问", Q8 and Q9.4.  Tile choices are
+found by a search over candidates measured on the real shapes (Q4: the fwd,
+bwd and tgmm phases each get their own tiling). A candidate may win only
+after an accuracy check, which a caller can loosen but never switch off.
 
-The space is the library's ``gmm_fp8_tile_config``:
-- ``bn``: the MMA N of a work unit, 128 or 256;
-- ``ctas``: the number of persistent CTAs;
-- ``unit_order``: the order of the work units, 1 row-tile major, 2 column-block major.
+The spaces are the library's tile configurations:
+- ``gmm_fp8_tile_config`` (``fp8_space``): ``bn`` the weight columns of a
+  work unit (128, 256); ``ctas`` the persistent CTAs; ``unit_order`` (1
+  row-tile major, 2 column-block major); ``cta_group`` (1 one CTA per 128-row
+  tile, 2 CTA pairs on 256-row tiles); ``stages`` the slots of the operand
+  ring; ``tmem_bufs`` the TMEM partial buffers the MMA rotates through.
+- ``gmm_tgmm_tile_config`` (``tgmm_space``): ``stages`` the CTA-pair
+  kernel's ring slots, ``claim_ahead`` the units its scheduler claims ahead of
+  the producer, ``max_batch`` the most small units per claim.
+Each field takes values from a list, and a rule (the same one the library
+applies before any launch) says which combinations exist.
 
 The search is evolutionary. The first population holds the default and random
-members. Each generation keeps the fastest members that pass the gate and
-fills up with mutants of them; a mutant has one field moved to a neighbouring
-value.
+valid members. Each generation keeps the fastest members that pass the gate
+and fills up with mutants of them: a mutant moves one field to a neighbouring
+value and, where the rule then forbids the combination, moves as few other
+fields as it must (by the smallest steps) to reach a valid one.
 
-The gate compares a candidate's output with the output of the default
-configuration. The test is bit for bit, since every configuration computes
-the same sums in the same order. A caller may loosen it to an atol/rtol bound.
+The gate compares a candidate's outputs with those of the default
+configuration, bit for bit: every configuration computes the same sums in
+the same order. A caller may loosen the FP8 gate to an atol/rtol bound.
+A candidate whose launch ran out a bounded wait fails the gate (its time is
+no measurement).
 
 Timing uses CUDA events on the launching stream, after one untimed run, with
 L2 flushed between runs. Everything measured runs in the library's kernels;
@@ -25,6 +35,7 @@ this module only chooses arguments.
 """
 from __future__ import annotations
 
+import itertools
 import random
 from dataclasses import dataclass, field
 
@@ -32,51 +43,102 @@ import torch
 
 from . import binding
 
-Config = tuple  # (bn, ctas, unit_order)
+Config = tuple
 
 
 @dataclass(frozen=True)
 class Space:
-    """The configurations a shape admits."""
-    bns: tuple
-    ctas: tuple
-    orders: tuple = (1, 2)
+    """A tile-configuration space: field names, the values each field may take
+    (in order, so that neighbours are adjacent), the default, and a rule
+    (config -> bool) for the combinations that exist."""
+    names: tuple
+    values: tuple
+    default: tuple
+    rule: object = None
+
+    def valid(self, c: Config) -> bool:
+        return self.rule is None or bool(self.rule(c))
 
     def contains(self, c: Config) -> bool:
-        return c[0] in self.bns and c[1] in self.ctas and c[2] in self.orders
+        return (len(c) == len(self.names) and all(v in vals for v, vals in zip(c, self.values))
+                and self.valid(c))
+
+    def members(self) -> list:
+        return [c for c in itertools.product(*self.values) if self.valid(c)]
+
+
+def _even(n: int) -> int:
+    return max(2, n - n % 2)
+
+
+def fp8_space(N: int, fuse: bool, sms: int) -> Space:
+    """gmm_fp8_tile_config for an output of N columns (fused: the gate/up
+    weight with 2N columns).  bn 256 needs N % 256 == 0 or the fused weight,
+    which has 256-column units only; CTA pairs need 256-column units and an
+    even CTA count; the ring slots and TMEM buffers are the compiled ones."""
+    bns = (256,) if fuse else ((128, 256) if N % 256 == 0 else (128,))
+    ctas = tuple(sorted({_even(sms * f // 8) for f in (4, 5, 6, 7, 8)}))
+    groups = (1, 2) if (fuse or N % 256 == 0) else (1,)
+
+    def rule(c):
+        bn, n_ctas, _, cg, st, tb = c
+        if cg == 2:
+            return bn == 256 and n_ctas % 2 == 0 and 3 <= st <= (5 if fuse else 4) and tb == 4
+        if bn == 256:
+            return st in (2, 3) and tb == 2
+        return st in (3, 4, 5) and tb in (2, 4)
+
+    bn0 = max(bns)
+    return Space(("bn", "ctas", "unit_order", "cta_group", "stages", "tmem_bufs"),
+                 (bns, ctas, (1, 2), groups, (2, 3, 4, 5), (2, 4)),
+                 (bn0, max(ctas), 1, 1, 3 if bn0 == 256 else 4, 2), rule)
+
+
+def tgmm_space(K: int, N: int) -> Space:
+    """gmm_tgmm_tile_config for dW [K, N]: the ring depth is selectable for
+    the CTA-pair kernel with 256-column units (K % 256 == 0, N % 256 == 0)."""
+    stages = (4, 5, 6) if (K % 256 == 0 and N % 256 == 0) else (6,)
+    return Space(("stages", "claim_ahead", "max_batch"), (stages, (1, 2, 3, 4, 6, 8), (1, 2, 4)), (6, 3, 4))
 
 
 def space_for(N: int, fuse: bool, sms: int) -> Space:
-    """bn 256 needs N % 256 == 0 and is the only value for the fused gate/up
-    weight; the CTA counts are the SM count and fractions of it."""
-    bns = (256,) if fuse else ((128, 256) if N % 256 == 0 else (128,))
-    ctas = tuple(sorted({max(1, sms * f // 8) for f in (4, 5, 6, 7, 8)}))
-    return Space(bns, ctas)
+    return fp8_space(N, fuse, sms)
 
 
 def default_config(space: Space) -> Config:
-    return (max(space.bns), max(space.ctas), 1)
+    return space.default
 
 
 def random_config(space: Space, rng: random.Random) -> Config:
-    return (rng.choice(space.bns), rng.choice(space.ctas), rng.choice(space.orders))
+    return rng.choice(space.members())
 
 
 def mutate(c: Config, space: Space, rng: random.Random) -> Config:
-    """Move one field (of those with a choice) to an adjacent allowed value."""
-    axes = [a for a, vals in enumerate((space.bns, space.ctas, space.orders)) if len(vals) > 1]
-    if not axes:
-        return c
-    a = rng.choice(axes)
-    vals = (space.bns, space.ctas, space.orders)[a]
-    i = vals.index(c[a])
-    j = i + rng.choice((-1, 1))
-    j = min(max(j, 0), len(vals) - 1)
-    if j == i:
-        j = i - 1 if i > 0 else i + 1
-    out = list(c)
-    out[a] = vals[j]
-    return tuple(out)
+    """Move one field (of those with a choice) to an adjacent value; when the
+    rule forbids the result, move the fewest other fields, by the smallest
+    steps, to a valid combination.  Returns c itself only when no field can
+    move."""
+    moves = []
+    for a, vals in enumerate(space.values):
+        i = vals.index(c[a])
+        for j in (i - 1, i + 1):
+            if 0 <= j < len(vals):
+                moves.append((a, vals[j]))
+    rng.shuffle(moves)
+    members = space.members()
+    for a, v in moves:
+        cands = [m for m in members if m[a] == v]
+        if not cands:
+            continue
+
+        def cost(m, a=a):
+            changed = [k for k in range(len(c)) if k != a and m[k] != c[k]]
+            steps = sum(abs(space.values[k].index(m[k]) - space.values[k].index(c[k])) for k in changed)
+            return (len(changed), steps)
+
+        best = min(cost(m) for m in cands)
+        return rng.choice([m for m in cands if cost(m) == best])
+    return c
 
 
 @dataclass
@@ -130,6 +192,43 @@ def status_passes(status: int, where: str = "") -> bool:
     return status == binding.GMM_OK
 
 
+def _measure(space, work, st, dev, run, alloc, same, reps, generations, population, keep, seed) -> Result:
+    """The search with the gate against the default configuration's outputs:
+    run(config, outs) launches; alloc() -> fresh outputs; same(outs, ref)."""
+    ref = alloc()
+    run(None, ref)
+    st.synchronize()
+    status = work.status(st)
+    if status != binding.GMM_OK:
+        raise RuntimeError(f"default configuration: {binding.STATUS_NAMES.get(status, status)}")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def evaluate(c):
+        outs = alloc()
+        run(c, outs)
+        st.synchronize()
+        ok = status_passes(work.status(st), f"config {c}") and same(outs, ref)
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            torch.cuda.current_stream(dev).synchronize()  # the flush, before the timed launch
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            run(c, outs)
+            e1.record(st)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ok = status_passes(work.status(st), f"config {c}, timed runs") and ok
+        times.sort()
+        return times[len(times) // 2], bool(ok)
+
+    return evolve(evaluate, space, generations, population, keep, seed)
+
+
+def _same_bits(outs, ref):
+    return all(torch.equal(a.view(torch.uint8), b.view(torch.uint8)) for a, b in zip(outs, ref))
+
+
 def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = False, generations: int = 4,
                  population: int = 6, keep: int = 2, seed: int = 0, reps: int = 5, atol: float | None = None,
                  rtol: float | None = None, stream=None) -> Result:
@@ -148,7 +247,7 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
     G, Nw, _ = wq.shape
     N = Nw // 2 if fuse else Nw
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    space = space_for(N, fuse, sms)
+    space = fp8_space(N, fuse, sms)
     st = torch.cuda.current_stream(dev) if stream is None else stream
     work = binding.group_metadata(group_sizes, M, stream=st)
 
@@ -165,53 +264,43 @@ def tune_fp8_fwd(xq, xs, wq, ws, group_sizes, fuse: bool = False, quant: bool = 
                     torch.empty((N // 128, M), dtype=torch.float32, device=dev))
         return (torch.empty((M, N), dtype=torch.bfloat16, device=dev),)
 
-    ref = alloc()
-    run(None, ref)
-    st.synchronize()  # the comparisons below run on torch's current stream
-    status = work.status(st)
-    if status != binding.GMM_OK:
-        raise RuntimeError(f"default configuration: {binding.STATUS_NAMES.get(status, status)}")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def same_bits(a, b):
-        return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
-
-    def device_ok(where):
-        return status_passes(work.status(st), where)
-
-    def evaluate(c):
-        outs = alloc()
-        run(c, outs)
-        st.synchronize()
-        ok = device_ok(f"config {c}")
+    def same(outs, ref):
         if quant or (atol is None and rtol is None):
-            ok = ok and all(same_bits(a, b) for a, b in zip(outs, ref))
-        else:
-            ok = ok and torch.allclose(outs[0].float(), ref[0].float(), atol=atol or 0.0, rtol=rtol or 0.0)
-        times = []
-        for _ in range(reps):
-            flush.zero_()
-            torch.cuda.current_stream(dev).synchronize()  # the flush, before the timed launch
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            run(c, outs)
-            e1.record(st)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1))
-        ok = device_ok(f"config {c}, timed runs") and ok
-        times.sort()
-        return times[len(times) // 2], bool(ok)
+            return _same_bits(outs, ref)
+        return torch.allclose(outs[0].float(), ref[0].float(), atol=atol or 0.0, rtol=rtol or 0.0)
 
-    return evolve(evaluate, space, generations, population, keep, seed)
+    return _measure(space, work, st, dev, run, alloc, same, reps, generations, population, keep, seed)
+
+
+def tune_tgmm(x, dy, group_sizes, generations: int = 4, population: int = 6, keep: int = 2, seed: int = 0,
+              reps: int = 5, stream=None) -> Result:
+    """Search gmm_tgmm_tile_config for dW = X_g^T dY_g on the current device;
+    the gate compares dW with the default configuration's bit for bit."""
+    dev = x.device
+    M, K = x.shape
+    _, N = dy.shape
+    G = group_sizes.numel()
+    space = tgmm_space(K, N)
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    work = binding.group_metadata(group_sizes, M, stream=st)
+
+    def run(c, outs):
+        binding.tgmm(x, dy, None, dw=outs[0], workspace=work, stream=st, config=c)
+
+    def alloc():
+        return (torch.empty((G, K, N), dtype=torch.bfloat16, device=dev),)
+
+    return _measure(space, work, st, dev, run, alloc, _same_bits, reps, generations, population, keep, seed)
 
 
 def main(argv=None):
-    """Tune the production MoE layer's two FP8 launches on this GPU and print
-    every measured configuration: the fused wi (G=256, M=65536, K=2048, W with
-    2 x 512 columns, writing h and its FP8 cast) and wo (K=512, N=2048 on the
-    FP8 cast of h).
+    """Tune the production MoE layer's launches on this GPU and print every
+    measured configuration: the fused wi (G=256, M=65536, K=2048, W with
+    2 x 512 columns, writing h and its FP8 cast), wo (K=512, N=2048 on the
+    FP8 cast of h), and the two weight gradients (dW_wo = h^T dY with
+    K=512, N=2048; dW_wi = X^T dH with K=2048, N=1024).
     Inputs are the seeded synthetic production workload (Zipf(1.1) top-8
-    routing, X N(0,1) with 1% x50 outliers, W N(0, 1/K))."""
+    routing, X N(0,1) with 1% x50 outliers, W N(0, 1/K), dY and dH N(0,1))."""
     import argparse
     import json
     import math
@@ -225,7 +314,9 @@ def main(argv=None):
     ap.add_argument("--population", type=int, default=6)
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--only", default=None, help="comma-separated subset of wi_fused_cast,wo,tgmm_wo,tgmm_wi")
     args = ap.parse_args(argv)
+    only = set(args.only.split(",")) if args.only else None
     dev = torch.device("cuda:0")
     G, M, K, N = 256, 65536, 2048, 512
     gen = torch.Generator(device=dev).manual_seed(1234)
@@ -237,17 +328,30 @@ def main(argv=None):
     xq, xs = binding.quantize_lhs(x)
     wq_wi, ws_wi = binding.quantize_rhs(w_wi)
     wq_wo, ws_wo = binding.quantize_rhs(w_wo)
-    _, hq, hs = binding.fp8_fwd_swiglu_quant(xq, xs, wq_wi, ws_wi, sizes, with_h=False)
+    del w_wi, w_wo
+    h, hq, hs = binding.fp8_fwd_swiglu_quant(xq, xs, wq_wi, ws_wi, sizes)
     out = {}
-    for name, a, quant in [("wi_fused_cast", (xq, xs, wq_wi, ws_wi), True), ("wo", (hq, hs, wq_wo, ws_wo), False)]:
-        r = tune_fp8_fwd(*a, sizes, quant=quant, generations=args.generations, population=args.population,
-                         reps=args.reps, seed=args.seed)
-        out[name] = {"best": list(r.best), "best_us": round(r.best_ms * 1e3, 1), "default": list(r.default),
-                     "default_us": round(r.default_ms * 1e3, 1),
+
+    def record(name, r, fields):
+        out[name] = {"fields": list(fields), "best": list(r.best), "best_us": round(r.best_ms * 1e3, 1),
+                     "default": list(r.default), "default_us": round(r.default_ms * 1e3, 1),
                      "measured": [{"generation": g, "config": list(c), "us": round(ms * 1e3, 1), "passed": ok}
                                   for g, c, ms, ok in r.history]}
-    print(json.dumps({"device": torch.cuda.get_device_name(dev), "config_fields": ["bn", "ctas", "unit_order"],
-                      **out}, indent=1))
+
+    kw = dict(generations=args.generations, population=args.population, reps=args.reps, seed=args.seed)
+    fp8_fields = fp8_space(N, True, 2).names
+    for name, a, quant in [("wi_fused_cast", (xq, xs, wq_wi, ws_wi), True), ("wo", (hq, hs, wq_wo, ws_wo), False)]:
+        if only is None or name in only:
+            record(name, tune_fp8_fwd(*a, sizes, quant=quant, **kw), fp8_fields)
+    tgmm_fields = tgmm_space(256, 256).names
+    if only is None or "tgmm_wo" in only:
+        dy = torch.randn(M, K, device=dev, generator=gen).to(torch.bfloat16)
+        record("tgmm_wo", tune_tgmm(h, dy, sizes, **kw), tgmm_fields)
+        del dy
+    if only is None or "tgmm_wi" in only:
+        dh = torch.randn(M, 2 * N, device=dev, generator=gen).to(torch.bfloat16)
+        record("tgmm_wi", tune_tgmm(x, dh, sizes, **kw), tgmm_fields)
+    print(json.dumps({"device": torch.cuda.get_device_name(dev), **out}, indent=1))
 
 
 if __name__ == "__main__":

@@ -174,6 +174,13 @@ gmm_status gmm_fp8_fwd(const void* xq, const float* xs, const void* wq, const fl
  *               into four TMEM buffers, the weight tile split between the
  *               pair (needs N % 256 == 0 or fuse_silu_mul = 1, bn 0 or 256
  *               and an even ctas)
+ *   stages      slots of the shared-memory operand ring: cta_group 1 with
+ *               bn 256: 2 or 3 (default 3); with bn 128: 3, 4 (default) or 5;
+ *               cta_group 2: 3 to 5 (default 5) fused, 3 or 4 (default 4)
+ *               otherwise
+ *   tmem_bufs   TMEM partial buffers the MMA rotates through: 2 with bn 256,
+ *               2 (default) or 4 with bn 128 (then all 512 TMEM columns), 4
+ *               for cta_group 2
  * A value outside these returns GMM_ERR_UNSUPPORTED before any launch.
  */
 typedef struct {
@@ -181,6 +188,8 @@ typedef struct {
   int ctas;
   int unit_order;
   int cta_group;
+  int stages;
+  int tmem_bufs;
 } gmm_fp8_tile_config;
 
 /*
@@ -290,6 +299,31 @@ gmm_status gmm_bf16_dgrad(const void* dy, const void* w, const int32_t* group_si
 gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M,
                      int64_t K, int64_t N, void* dw, void* workspace, size_t workspace_bytes,
                      void* stream);
+
+/*
+ * Tile configuration of tgmm_bf16, the space the autotuner searches for it
+ * ("GEMM Kernel 性能优化十问", Q4: the fwd, bwd and tgmm phases each get their
+ * own tiling; Q8: chosen by a search over measured candidates).  The fields
+ * apply to the CTA-pair kernel (K % 256 == 0); every configuration computes
+ * the same sums in the same order.  A field left 0 keeps the default.
+ *   stages       slots of its operand ring with 256-column units (N % 256 ==
+ *                0): 4, 5 or 6 (default 6); 128-column units always use 8
+ *   claim_ahead  units the pair's scheduler claims beyond those its producer
+ *                has started: 1..12 (default 3)
+ *   max_batch    most units one claim takes once the units are small (the
+ *                units come largest first): 1..4 (default 4)
+ * A value outside these returns GMM_ERR_UNSUPPORTED before any launch.
+ */
+typedef struct {
+  int stages;
+  int claim_ahead;
+  int max_batch;
+} gmm_tgmm_tile_config;
+
+/* tgmm_bf16 with a tile configuration (config = NULL: exactly tgmm_bf16). */
+gmm_status tgmm_bf16_tiled(const void* x, const void* dy, const int32_t* group_sizes, int G, int64_t M,
+                           int64_t K, int64_t N, void* dw, void* workspace, size_t workspace_bytes,
+                           void* stream, const gmm_tgmm_tile_config* config);
 
 /*
  * gmm_fp8_fwd without a workspace argument, for callers that cannot allocate

@@ -103,10 +103,23 @@ def _tiled(lib, cfg, **kw):
     # CTA pairs: 256-column units (not with bn 128 or N % 256 != 0), even CTA counts
     ((0, 0, 0, 2), dict(N=384), 4), ((128, 0, 0, 2), {}, 4), ((0, 7, 0, 2), {}, 4), ((0, 0, 0, 3), {}, 4),
     ((0, 0, 0, -1), {}, 4),
+    # compiled ring depths and TMEM buffer counts only
+    ((256, 0, 0, 1, 4, 0), {}, 4), ((128, 0, 0, 1, 2, 0), {}, 4), ((0, 0, 0, 0, 0, 3), {}, 4),
+    ((256, 0, 0, 1, 0, 4), {}, 4), ((0, 0, 0, 2, 5, 0), {}, 4), ((0, 0, 0, 2, 0, 2), {}, 4),
+    ((0, 0, 0, 0, -1, 0), {}, 4),
 ])
 def test_tile_config_host_validation(lib, cfg, kw, code):
     # rejected on the host, before any device call
     assert _tiled(lib, cfg, **kw) == code
+
+
+@pytest.mark.parametrize("cfg", [(3, 0, 0), (7, 0, 0), (0, 13, 0), (0, -1, 0), (0, 0, 5), (0, 0, -2)])
+def test_tgmm_config_host_validation(lib, cfg):
+    import ctypes
+    from fp8_blockwise_quantized_gb300 import TgmmConfig
+    # rejected on the host, before any device call
+    assert lib.tgmm_bf16_tiled(FAKE, FAKE, FAKE, 4, 512, 256, 256, FAKE, FAKE, 1 << 20, None,
+                               ctypes.byref(TgmmConfig(*cfg))) == 4
 
 
 def test_null_group_sizes_is_not_a_host_error(lib):

@@ -1,9 +1,11 @@
-"""The FP8 forward's tile configurations on the GPU: every configuration the
-autotuner may choose gives the default configuration's bits (the same sums in
-the same order), on ragged cases with empty groups, partial tiles and tail
-rows, plain and fused; the device-dependent configuration errors; and one
-short autotuner run whose winner passes the gate.  The default configuration
-itself is checked against the oracle in test_gpu_gmm.py."""
+"""The tile configurations on the GPU: every configuration the autotuner may
+choose (FP8 forward: bn, CTA count, unit order, CTA group, ring slots, TMEM
+buffers; tgmm: ring slots, claim-ahead, claim batch) gives the default
+configuration's bits (the same sums in the same order), on ragged cases with
+empty groups, partial tiles and tail rows, plain, fused and with the fused
+FP8 cast; the device-dependent configuration errors; and short autotuner runs
+whose winners pass the gate.  The default configurations themselves are
+checked against the oracle in test_gpu_gmm.py and test_gpu_tgmm.py."""
 import numpy as np
 import pytest
 import torch
@@ -45,28 +47,58 @@ def test_every_config_gives_the_default_bits(sizes, M, K, N):
     s, xq, xs, wq, ws = _problem(sizes, M, K, N, 5 + M)
     ref = gmm.fp8_fwd(xq, xs, wq, ws, s)
     sms = _sms()
-    bns = (128, 256) if N % 256 == 0 else (128,)
-    for bn in bns:
-        for ctas in (0, 1, 7, sms // 2, sms):
-            for order in (1, 2):
-                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(bn, ctas, order, 1))
-                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (bn, ctas, order, 1)
-    if N % 256 == 0:  # CTA pairs: 256-column units, an even CTA count
-        for ctas in (0, 2, 8, _even(sms // 2), sms):
-            for order in (1, 2):
-                got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=(256, ctas, order, 2))
-                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (256, ctas, order, 2)
+    # every member of the autotuner's space (bn, CTA count, unit order, CTA
+    # group, ring slots, TMEM buffers), plus a few small CTA counts
+    cfgs = tune.fp8_space(N, False, sms).members()
+    cfgs += [(128, c, 1, 1, 4, 2) for c in (1, 7)] + [(128, 3, 2, 1, 5, 4)]
+    if N % 256 == 0:
+        cfgs += [(256, 1, 1, 1, 3, 2), (256, 2, 2, 2, 3, 4), (256, 8, 1, 2, 4, 4)]
+    for cfg in cfgs:
+        got = gmm.fp8_fwd(xq, xs, wq, ws, s, config=cfg)
+        assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), cfg
 
 
 def test_fused_configs_give_the_default_bits():
     sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
     s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 17)
     ref = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True)
-    for cg, ctas_list in ((1, (0, 3, _sms() // 2)), (2, (0, 2, _even(_sms() // 2)))):
-        for ctas in ctas_list:
-            for order in (1, 2):
-                got = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=(256, ctas, order, cg))
-                assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), (ctas, order, cg)
+    for cfg in tune.fp8_space(N, True, _sms()).members() + [(256, 3, 1, 1, 2, 2), (256, 2, 2, 2, 5, 4)]:
+        got = gmm.fp8_fwd(xq, xs, wq, ws, s, fuse=True, config=cfg)
+        assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), cfg
+
+
+def test_tgmm_configs_give_the_default_bits():
+    """Every ring depth, claim-ahead and claim batch of the CTA-pair tgmm
+    kernel gives the default's dW bits (the same sums in the same order), on
+    many small groups (batched claims), a large one and empty ones; the work
+    counters are back at zero after every launch."""
+    rng = np.random.default_rng(71)
+    G, K, N = 300, 512, 256
+    sizes = np.where(rng.random(G) < 0.3, 0, rng.integers(1, 40, G)).astype(np.int32)
+    sizes[[3, 100]] = [900, 257]
+    M = int(sizes.sum()) + 9
+    x = to_dev_bf16(normal_bf16((M, K), 1.0, rng))
+    dy = to_dev_bf16(normal_bf16((M, N), 1.0, rng))
+    sd = to_dev(sizes)
+    work = gmm.Workspace(G, M)
+    ref = gmm.tgmm(x, dy, sd, workspace=work)
+    for cfg in tune.tgmm_space(K, N).members():
+        got = gmm.tgmm(x, dy, sd, workspace=work, config=cfg)
+        torch.cuda.synchronize()
+        assert torch.equal(ref.view(torch.int16), got.view(torch.int16)), cfg
+        assert work.buf[16:24].view(torch.int32).tolist() == [0, 0], cfg
+    assert work.status() == 0
+
+
+def test_tgmm_autotuner_winner_passes_the_gate():
+    rng = np.random.default_rng(72)
+    sizes = np.array([700, 0, 3, 260, 129, 64, 1, 900], np.int32)
+    M, K, N = int(sizes.sum()), 512, 512
+    x = to_dev_bf16(normal_bf16((M, K), 1.0, rng))
+    dy = to_dev_bf16(normal_bf16((M, N), 1.0, rng))
+    r = tune.tune_tgmm(x, dy, to_dev(sizes), generations=2, population=4, reps=2, seed=3)
+    assert tune.tgmm_space(K, N).contains(r.best) and r.default == (6, 3, 4)
+    assert all(ok for _, _, _, ok in r.history)
 
 
 def test_config_errors_on_the_device():
@@ -91,7 +123,7 @@ def test_autotuner_winner_passes_the_gate():
     sizes, M, K, N = [700, 0, 3, 260, 129, 64, 1, 900], 2100, 512, 512
     s, xq, xs, wq, ws = _problem(sizes, M, K, N, 23)
     r = tune.tune_fp8_fwd(xq, xs, wq, ws, s, generations=2, population=4, reps=2, seed=1)
-    sp = tune.space_for(N, False, _sms())
+    sp = tune.fp8_space(N, False, _sms())
     assert sp.contains(r.best) and r.default == tune.default_config(sp)
     assert all(ok for _, _, _, ok in r.history)  # every configuration gives the default's bits
     ref = gmm.fp8_fwd(xq, xs, wq, ws, s)
@@ -106,12 +138,10 @@ def test_fused_cast_configs_give_the_default_bits():
     sizes, M, K, N = [300, 0, 129, 1, 640], 1200, 512, 256
     s, xq, xs, wq, ws = _problem(sizes, M, K, 2 * N, 29)
     ref = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s)
-    for cg, ctas_list in ((1, (0, 5, _sms() // 2)), (2, (0, 4, _even(_sms() // 2)))):
-        for ctas in ctas_list:
-            for order in (1, 2):
-                got = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(256, ctas, order, cg))
-                for a, b in zip(ref, got):
-                    assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (ctas, order, cg)
+    for cfg in tune.fp8_space(N, True, _sms()).members() + [(256, 5, 1, 1, 2, 2), (256, 4, 2, 2, 3, 4)]:
+        got = gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=cfg)
+        for a, b in zip(ref, got):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), cfg
     with pytest.raises(gmm.GmmError) as e:
         gmm.fp8_fwd_swiglu_quant(xq, xs, wq, ws, s, config=(128, 0, 1))
     assert e.value.status == 4
