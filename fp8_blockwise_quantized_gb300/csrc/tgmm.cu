@@ -337,13 +337,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 //              the pair's TMEM buffer by remote arrives on the even CTA.
 //   warp 10    even CTA: the pair's scheduler (below).
 // Scheduling: the units are numbered largest groups first and the pairs
-// claim them from a counter in the workspace as they go (list scheduling in
-// decreasing size), so a pair that runs slower, or drew larger units, takes
-// fewer.  The scheduler claims a few units ahead of the producer (one claim
-// in flight while the previous one is resolved, several small units per claim
-// once the units get small) and puts each unit {g, rem, r0, r1} in a queue of kQueue entries in
-// its own shared memory and, by a bulk copy that completes on the odd CTA's
-// barrier, in the odd CTA's.  Every role of both CTAs takes the units from
+// claim them from a counter in the workspace as they go (list scheduling; a
+// pair that runs slower, or drew larger units, takes fewer).  With skewed
+// group sizes the claims alternate between the large and the small end of
+// that order, so that long, read-heavy units and short, store-heavy ones run
+// side by side.  The scheduler claims only while few chunks are queued ahead
+// of its producer (several small units per claim once the units get small)
+// and puts each unit {g, rem, r0, r1} in a queue of kQueue entries in its own
+// shared memory and, by a bulk copy that completes on the odd CTA's barrier,
+// in the odd CTA's.  Every role of both CTAs takes the units from
 // its queue in the same order and frees an entry on the even CTA once it has
 // read it.  The last CTA to finish resets the counters for the next launch.
 constexpr int kPairStages = 6;  // default ring slots with BN = 256 (4 or 5 selectable)
@@ -351,9 +353,10 @@ constexpr int kPairThreads = 352;
 constexpr int kSchedWarp = 10;
 constexpr int kQueue = 16;
 constexpr int kQueueReaders = 2 * (2 + kEpiWarps);  // producer, warp 1, epilogue warps; both CTAs
-// the scheduler claims at most TgmmArgs::claim_ahead units (default 3) beyond
-// those the even CTA's producer has taken, and up to TgmmArgs::max_batch
-// (1..kMaxBatch, default 4) small units per claim
+// the scheduler holds at most TgmmArgs::claim_ahead units (default 3) beyond
+// those the even CTA's producer has taken, claims only while fewer than 8
+// chunks are queued ahead of that producer, and takes up to
+// TgmmArgs::max_batch (1..kMaxBatch, default 4) small units per claim
 
 // Zero rows [from, to) of both 64-row x boxes of a ring slot (128 bytes per
 // row and box, so the swizzle does not matter) and fence them into the async
@@ -378,7 +381,7 @@ struct TgmmPairTile {
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kStagingBytes = kEpiWarps * 4096;
   // queue entries (16 bytes each), then the barriers, the TMEM address and the abort word
-  static constexpr int kTailBytes = 16 * kQueue + 8 * (3 * kStages + 5 + 2 * kQueue) + 12;
+  static constexpr int kTailBytes = 16 * kQueue + 8 * (3 * kStages + 5 + 2 * kQueue) + 16;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 1024;
   static_assert(kTailBytes <= 1024, "barrier area");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -433,12 +436,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qempty + kQueue);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* taken = abort_word + 1;  // even CTA: queue entries its producer has taken
+  volatile int* ctaken = taken + 1;      // even CTA: chunks its producer has issued (1 per empty unit)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   if (threadIdx.x == 0) {
     *taken = 0;
+    *ctaken = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 2);
       mbar_init(&ploaded[s], 1);
@@ -484,9 +489,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t c = 0;
       bool ok = true;
       int4 e;
+      int issued = 0;
       for (uint32_t i = 0; ok && queue.get(i, e, false, 0, abort_word, lim) && e.x >= 0; ++i) {
         *taken = static_cast<int>(i) + 1;
         const int rem = e.y, r0 = e.z, r1 = e.w;
+        if (r1 <= r0) *ctaken = ++issued;  // an empty group's unit counts as one chunk
         const int k0 = (rem / NT) * 256 + static_cast<int>(rank) * 128;
         const int n0 = (rem % NT) * BN + static_cast<int>(rank) * (BN / 2);
         for (int r = r0; r < r1; r += kChunk) {
@@ -522,6 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               tma_load_2d_pair(b_dst + i2 * C::kBoxBytes, &map_dy, bar, n0 + 64 * i2, r);
           }
           ++c;
+          *ctaken = ++issued;
         }
       }
       // the even CTA waits for the last copies into every slot (they land in
@@ -693,27 +701,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       return true;
     };
     constexpr int kMaxBatch = 4;
+    // Claim q takes unit q/2 from the large end of the size order when q is
+    // even and unit num_units-1-q/2 from the small end when q is odd, so every
+    // pair alternates long, read-heavy units with short ones whose cost is
+    // mostly the dW store (or only that, for an empty group): the loads of the
+    // one overlap the stores of the other, and the launch never runs a phase of
+    // loads only followed by a phase of stores only.
+    // With groups of about one size there is nothing to mix, and the plain
+    // order keeps each group's units together: alternate only when the
+    // largest group has more than twice the chunks of the smallest.
+    bool mix = false;
+    if (num_units > 0) {
+      const int gl = __ldg(args.order), gs = __ldg(args.order + args.G - 1);
+      const int cl = (__ldg(offsets + gl + 1) - __ldg(offsets + gl) + kChunk - 1) / kChunk;
+      const int cs = (__ldg(offsets + gs + 1) - __ldg(offsets + gs) + kChunk - 1) / kChunk;
+      mix = cl > 2 * cs;
+    }
+    auto unit_of = [&](int q) { return (mix && (q & 1)) ? num_units - 1 - (q >> 1) : (mix ? (q >> 1) : q); };
+    // Claims are paced by work: the next claim is made only once the producer
+    // is within kLeadChunks chunks of the end of what is already published, so
+    // that a claimed unit starts within a few microseconds (the units of one
+    // group, claimed one after the other, then read its rows at about the same
+    // time and find them in L2, instead of one of them waiting behind a long
+    // unit and reading them again after they were evicted).
+    constexpr int kLeadChunks = 8;
     bool ok = true;
-    int batch = 1, next_batch = 1;
-    int k = num_units > 0 ? atomicAdd(claimed, 1) : num_units;
-    while (ok && k < num_units) {
-      const int k0 = k, cnt = min(batch, num_units - k0);
-      k = atomicAdd(claimed, next_batch);  // the next claim is in flight while this one is resolved
-      batch = next_batch;
-      int g[kMaxBatch], r0[kMaxBatch], r1[kMaxBatch];
+    int batch = min(mix ? 2 : 1, args.max_batch);
+    int published = 0;  // chunks of the published units (1 for an empty group's)
+    while (ok) {
+      if (published - *ctaken >= kLeadChunks) {
+        const uint64_t t0 = global_timer_ns();
+        while (published - *ctaken >= kLeadChunks) {
+          if (*abort_word || global_timer_ns() - t0 > lim) break;
+          __nanosleep(64);
+        }
+        if (*abort_word || published - *ctaken >= kLeadChunks) {
+          *abort_word = 1;
+          ok = false;
+          break;
+        }
+      }
+      const int k0 = atomicAdd(claimed, batch);
+      if (k0 >= num_units) break;
+      const int cnt = min(batch, num_units - k0);
+      int u[kMaxBatch], g[kMaxBatch], r0[kMaxBatch], r1[kMaxBatch];
 #pragma unroll
-      for (int j = 0; j < kMaxBatch; ++j) g[j] = j < cnt ? __ldg(args.order + (k0 + j) / KPNT) : 0;
+      for (int j = 0; j < kMaxBatch; ++j) u[j] = j < cnt ? unit_of(k0 + j) : 0;
+#pragma unroll
+      for (int j = 0; j < kMaxBatch; ++j) g[j] = j < cnt ? __ldg(args.order + u[j] / KPNT) : 0;
 #pragma unroll
       for (int j = 0; j < kMaxBatch; ++j) {
         r0[j] = j < cnt ? __ldg(offsets + g[j]) : 0;
         r1[j] = j < cnt ? __ldg(offsets + g[j] + 1) : 0;
       }
 #pragma unroll
-      for (int j = 0; j < kMaxBatch; ++j)
-        if (ok && j < cnt) ok = publish(make_int4(g[j], (k0 + j) % KPNT, r0[j], r1[j]));
-      // the units come largest first: claim more at once as they get small
-      const int chunks = (r1[cnt - 1] - r0[cnt - 1] + kChunk - 1) / kChunk;
-      next_batch = chunks >= 4 ? 1 : chunks >= 2 ? min(2, args.max_batch) : args.max_batch;
+      for (int j = 0; j < kMaxBatch; ++j) {
+        if (ok && j < cnt) {
+          ok = publish(make_int4(g[j], u[j] % KPNT, r0[j], r1[j]));
+          published += max(1, (r1[j] - r0[j] + kChunk - 1) / kChunk);
+        }
+      }
+      // the large-end units shrink as the claims go on: claim more at once
+      // when they get small (when mixing, the first claim of the batch is a
+      // large-end one whenever the batch size is even)
+      const int jf = (mix && (k0 & 1)) ? (cnt > 1 ? 1 : 0) : 0;
+      const int chunks = (r1[jf] - r0[jf] + kChunk - 1) / kChunk;
+      batch = min(chunks >= 4 ? (mix ? 2 : 1) : chunks >= 2 ? 2 : 4, args.max_batch);
     }
     if (ok) publish(make_int4(-1, 0, 0, 0));
   }

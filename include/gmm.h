@@ -308,10 +308,14 @@ gmm_status tgmm_bf16(const void* x, const void* dy, const int32_t* group_sizes, 
  * the same sums in the same order.  A field left 0 keeps the default.
  *   stages       slots of its operand ring with 256-column units (N % 256 ==
  *                0): 4, 5 or 6 (default 6); 128-column units always use 8
- *   claim_ahead  units the pair's scheduler claims beyond those its producer
- *                has started: 1..12 (default 3)
- *   max_batch    most units one claim takes once the units are small (the
- *                units come largest first): 1..4 (default 4)
+ *   claim_ahead  units the pair's scheduler may hold beyond those its
+ *                producer has started: 1..12 (default 3); independently of it
+ *                the scheduler claims only while fewer than 8 chunks (64 rows
+ *                each) are queued ahead of its producer
+ *   max_batch    most units one claim takes once the units are small: 1..4
+ *                (default 4).  The units are ordered largest group first; when
+ *                the largest group has more than twice the chunks of the
+ *                smallest, claims alternate between the two ends of that order
  * A value outside these returns GMM_ERR_UNSUPPORTED before any launch.
  */
 typedef struct {
