@@ -21,10 +21,13 @@
 //               N=BN, K=32, four per K block) into one of NBUF TMEM partial
 //               buffers (2; or 4 with BN = 128, all 512 columns);
 //               tcgen05.commit frees the ring slot and publishes the partial.
-//   warp 2      scale loader: per K block, cp.async copies of the tile's 128
-//               row scales xs[kb, rows] and its RHS block scales into a
-//               shared-memory ring that runs ahead of the MMAs (the scales are
-//               then never a global-memory load on the promotion's path).
+//   warp 2      unit scheduler and scale loader: claims the CTA's next unit
+//               from a counter in the workspace and hands it to the other
+//               roles through a shared-memory queue; then, per K block,
+//               cp.async copies of the tile's 128 row scales xs[kb, rows] and
+//               its RHS block scales into a shared-memory ring that runs ahead
+//               of the MMAs (the scales are then never a global-memory load on
+//               the promotion's path).
 //   warp 3      store warp: takes each unit's staged bf16 output boxes to
 //               global memory (TMA tensor stores for full 32-row boxes, masked
 //               stores for ragged ones: the tile may run into the next group)
@@ -36,15 +39,16 @@
 //               bf16 (silu(gate) * up when fused) into swizzled 32x64 staging
 //               boxes and go on with the next unit while the store warp
 //               drains them.  They also zero the output rows no group covers.
-// Work units (tile, column block) are dealt round-robin to a persistent grid
-// of one CTA per SM, tile-major so that the units sharing an Xq tile and the
-// tiles sharing an expert's Wq columns run at the same time (L2 reuse).
+// Work units (tile, column block) are claimed by a persistent grid of one CTA
+// per SM from a counter as the CTAs go (list scheduling: a CTA that runs
+// slower takes fewer), numbered tile-major so that the units sharing an Xq
+// tile and the tiles sharing an expert's Wq columns run at the same time (L2
+// reuse).  The last CTA to finish resets the counter for the next launch.
 // Every wait is bounded; a timeout sets the workspace error word and all
 // roles unwind, wait for their copies and MMAs in flight and free TMEM.
 #include "common.cuh"
 #include "kernels.cuh"
 #include "ptx.cuh"
-#include "tilewalk.cuh"
 
 namespace gmm {
 
@@ -65,6 +69,29 @@ struct RegSplit {
 };
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kScaleSlots = 8;        // K blocks of scales in flight
+constexpr int kUnitSlots = 8;         // entries of the CTA's unit queue
+// readers of a queue entry: producer, MMA issuer, store warp, promotion warps
+constexpr int kUnitReaders = 3 + 8;
+
+// The CTA's unit queue: the scale loader claims each unit from a counter in
+// the workspace and writes {g, row0, row1, first output column} (g < 0: no
+// more units) to entry i % kUnitSlots; every other role takes the entries in
+// order and frees each one it has read.
+struct FwdUnitQueue {
+  uint64_t* full;
+  uint64_t* empty;
+  const int4* data;
+  __device__ bool get(uint32_t i, int4& e, bool warp_wide, int lane, volatile int* abort_word, uint64_t lim) const {
+    const uint32_t slot = i % kUnitSlots, ph = (i / kUnitSlots) & 1u;
+    bool ok = mbar_wait(&full[slot], ph, abort_word, lim);
+    if (warp_wide) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    e = data[slot];
+    if (warp_wide) __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    return true;
+  }
+};
 constexpr int kScaleSlotFloats = 132;  // 128 row scales + 2 block scales (+ pad)
 
 template <int BN, bool FUSE, bool QUANT, int STAGES, int NBUF>
@@ -84,11 +111,13 @@ struct Fp8Tile {
   static constexpr int kBufs = NBUF;                   // TMEM partial buffers (2, or 4 with BN = 128)
   static constexpr int kTmemCols = NBUF * BN;
   static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
-  static constexpr int kBarBytes = 512;
+  static constexpr int kBarBytes = 768;  // barriers, then the unit queue's entries
   static constexpr int kScaleBytes = kScaleSlots * kScaleSlotFloats * 4;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + kScaleBytes + kBarBytes;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(8 * (2 * kStages + 2 * NBUF + 2 * kScaleSlots + 3) + 8 <= kBarBytes, "barrier area");
+  static_assert(8 * (2 * kStages + 2 * NBUF + 2 * kScaleSlots + 3 + 2 * kUnitSlots) + 32 + 16 * kUnitSlots <=
+                    kBarBytes,
+                "barrier area");
 };
 
 template <int BN, bool FUSE, bool QUANT, int STAGES, int NBUF>
@@ -113,8 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* staged = sempty + kScaleSlots;  // a unit's output boxes are in the staging area
   uint64_t* sfree = staged + 1;             // the store warp has emptied the staging area
   uint64_t* drain = sfree + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ufull = drain + 1;          // unit queue entry written
+  uint64_t* uempty = ufull + kUnitSlots;  // unit queue entry read by every reader
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(uempty + kUnitSlots);
   volatile int* abort_word = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int4* udata = reinterpret_cast<int4*>((reinterpret_cast<uintptr_t>(tmem_slot + 2) + 15) & ~uintptr_t{15});
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -133,6 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(staged, kPromoWarps);
     mbar_init(sfree, 1);
     mbar_init(drain, 1);
+    for (int q = 0; q < kUnitSlots; ++q) {
+      mbar_init(&ufull[q], 1);
+      mbar_init(&uempty[q], kUnitReaders);
+    }
     *abort_word = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_a);
@@ -157,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int KB = args.K / 128;
   const int Nw = FUSE ? 2 * args.N : args.N;
   const uint64_t lim = args.wait_limit_ns;
+  const FwdUnitQueue queue{ufull, uempty, udata};
 
   if (warp < kPromoWarp0) regs_dec<RegSplit<BN>::kControl>();
   if (warp == 0) {
@@ -168,9 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t stage_tx = C::kABytes + (args.b_fmt != 0 ? C::kBBytes / 2 : C::kBBytes);
       uint32_t c = 0;
       bool ok = true;
-      for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
-        const Tile tl = w.cur;
-        const int n0 = w.col0(C::kOutCols);
+      int4 e;
+      for (uint32_t i = 0; ok && queue.get(i, e, false, 0, abort_word, lim) && e.x >= 0; ++i) {
+        const Tile tl{e.x, e.y, e.z, 0};
+        const int n0 = e.w;
         const int brow = tl.g * Nw + n0;
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
@@ -208,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           (make_idesc(0u /*e4m3*/, false, false, kBM, BN) & ~(7u << 10)) | (static_cast<uint32_t>(args.b_fmt) << 10);
       uint32_t c = 0, t = 0;
       bool ok = true;
-      for (uint32_t u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      int4 e;
+      for (uint32_t i = 0; ok && queue.get(i, e, false, 0, abort_word, lim) && e.x >= 0; ++i) {
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t s = c % kStages, ph = (c / kStages) & 1u;
           if (!mbar_wait(&full[s], ph, abort_word, lim)) {
@@ -242,13 +281,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ scale loader
+    // ------------------------------------------------------------ unit scheduler and scale loader
+    // Claims units from the workspace counter (units u = row tile u / per_tile,
+    // column block u % per_tile, or column-block major), one claim in flight
+    // while the current unit is published and its scales are loaded.
     const int NBw = Nw / 128;
+    int* claimed = const_cast<int32_t*>(args.meta) + kWsClaimed;
     uint32_t q = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
-      const Tile tl = w.cur;
-      const int n0 = w.col0(C::kOutCols);
+    int mine = 0;
+    if (lane == 0) mine = atomicAdd(claimed, 1);
+    for (uint32_t i = 0; ok; ++i) {
+      const int u = __shfl_sync(0xffffffffu, mine, 0);
+      const bool live = u < static_cast<int>(num_units);
+      if (live && lane == 0) mine = atomicAdd(claimed, 1);
+      int4 ent = make_int4(-1, 0, 0, 0);
+      if (live) {
+        const uint32_t tix = col_major ? static_cast<uint32_t>(u) % static_cast<uint32_t>(num_tiles)
+                                       : static_cast<uint32_t>(u) / static_cast<uint32_t>(units_per_tile);
+        const int col = col_major ? u / num_tiles : u % units_per_tile;
+        const int4 t = __ldg(reinterpret_cast<const int4*>(args.tiles + tix));
+        ent = make_int4(t.x, t.y, t.z, col * C::kOutCols);
+      }
+      {
+        const uint32_t slot = i % kUnitSlots, ph = (i / kUnitSlots) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&uempty[slot], ph ^ 1u, abort_word, lim))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          udata[slot] = ent;
+          mbar_arrive(&ufull[slot]);
+        }
+        __syncwarp();
+      }
+      if (!live) break;
+      const Tile tl{ent.x, ent.y, ent.z, 0};
+      const int n0 = ent.w;
       // the (up to) two RHS column blocks this unit's accumulators use
       const int wb0 = n0 / 128;
       const int wb1 = FUSE ? (args.N + n0) / 128 : (BN == 256 ? n0 / 128 + 1 : n0 / 128);
@@ -279,9 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ store warp
     uint32_t ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
-      const Tile tl = w.cur;
-      const int n0 = w.col0(C::kOutCols);
+    int4 e;
+    for (uint32_t i = 0; ok && queue.get(i, e, true, lane, abort_word, lim) && e.x >= 0; ++i) {
+      const Tile tl{e.x, e.y, e.z, 0};
+      const int n0 = e.w;
       if (!__all_sync(0xffffffffu, mbar_wait(staged, ue & 1u, abort_word, lim))) {
         ok = false;
         break;
@@ -392,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint32_t t = 0, ue = 0;
     bool ok = true;
-    for (TileWalk w(args.tiles, units_per_tile, num_units, num_tiles, col_major, blockIdx.x, gridDim.x); w.live() && ok; w.next()) {
-      const Tile tl = w.cur;
+    int4 e;
+    for (uint32_t i = 0; ok && queue.get(i, e, true, lane, abort_word, lim) && e.x >= 0; ++i) {
+      const Tile tl{e.x, e.y, e.z, 0};
       const int row = tl.row0 + quad * 32 + lane;
       const bool valid = row < tl.row1;
       int tcol0, tcol1, wsel0, wsel1;
@@ -506,7 +577,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, C::kTmemCols);
   }
-  if (threadIdx.x == 0 && *abort_word) atomicOr(const_cast<int32_t*>(args.meta) + kWsStatus, kErrTimeout);
+  if (threadIdx.x == 0) {
+    int32_t* w = const_cast<int32_t*>(args.meta);
+    if (*abort_word) atomicOr(w + kWsStatus, kErrTimeout);
+    // every CTA has stopped claiming; the last one out resets the counters
+    __threadfence();
+    if (atomicAdd(w + kWsFinished, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(w + kWsClaimed, 0);
+      atomicExch(w + kWsFinished, 0);
+    }
+  }
 }
 
 template <int BN, bool FUSE, bool QUANT, int STAGES, int NBUF>

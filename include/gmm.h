@@ -86,9 +86,10 @@ size_t gmm_workspace_bytes(int G, int64_t M);
  *   int32 word[1]  1 if this call's sizes were valid, else 0
  *   int32 word[2]  S = sum(group_sizes)        (M when invalid)
  *   int32 word[3]  T = number of row tiles      (0 when invalid)
- *   int32 word[4], word[5]  set to 0: the work counters of tgmm_bf16 (units
- *                  claimed, CTAs finished); each tgmm_bf16 launch claims its
- *                  units from them and its last CTA sets them back to 0
+ *   int32 word[4], word[5]  set to 0: the work counters of tgmm_bf16 and of
+ *                  the FP8 forward with one CTA per tile (units claimed, CTAs
+ *                  finished); each such launch claims its units from them and
+ *                  its last CTA sets them back to 0
  *   int32 word[6]  T2 = number of 256-row tiles (0 when invalid)
  *   int32 word[8 + g], g = 0..G  exclusive prefix sums off_g (off_G = S)
  *   int32x4 tiles[T] at byte offset gmm_tiles_offset(G): {g, row0, row1, 0},
