@@ -155,3 +155,32 @@ def test_repeated_calls_reuse_workspace():
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert work.status() == 0
+
+
+def test_claim_counters_shared_across_launches():
+    """The FP8 forward (one CTA per tile) and tgmm both claim their units from
+    the workspace's counter words and their last CTA resets them: a chain of
+    launches of both kinds on one workspace, reusing its metadata (group sizes
+    NULL), gives every launch the same bits as a fresh workspace, and the
+    counters are zero at the end."""
+    s, x, w = _inputs([700, 0, 3, 1300, 129, 0, 64], 2400, 512, 512, 11)
+    G, M = len(s), 2400
+    xd = to_dev_bf16(x)
+    xq, xs = gmm.quantize_lhs(xd)
+    wq, ws = gmm.quantize_rhs(to_dev_bf16(w))
+    dy = torch.randn(M, 256, device="cuda", generator=torch.Generator(device="cuda").manual_seed(3)).to(torch.bfloat16)
+    ref_y = gmm.fp8_fwd(xq, xs, wq, ws, to_dev(s), workspace=gmm.Workspace(G, M))
+    ref_h = gmm.fp8_fwd(xq, xs, wq, ws, to_dev(s), workspace=gmm.Workspace(G, M), fuse=True)
+    ref_dw = gmm.tgmm(xd, dy, to_dev(s), workspace=gmm.Workspace(G, M))
+    work = gmm.group_metadata(to_dev(s), M)
+    for _ in range(3):
+        y = gmm.fp8_fwd(xq, xs, wq, ws, None, workspace=work)
+        dw = gmm.tgmm(xd, dy, None, workspace=work)
+        h = gmm.fp8_fwd(xq, xs, wq, ws, None, workspace=work, fuse=True)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref_y.view(torch.int16))
+        assert torch.equal(h.view(torch.int16), ref_h.view(torch.int16))
+        assert torch.equal(dw.view(torch.int16), ref_dw.view(torch.int16))
+    assert work.status() == 0
+    words = work.buf[:32].view(torch.int32).cpu()
+    assert int(words[4]) == 0 and int(words[5]) == 0, "claim counters not reset"
