@@ -1,4 +1,5 @@
-// The FP8 kernels' walk over their work units.
+// The CTA-pair FP8 kernel's static walk over its work units (the single-CTA
+// kernel claims its units from a counter instead).
 #pragma once
 
 #include <cstdint>
